@@ -1,0 +1,451 @@
+#!/usr/bin/env python3
+"""Benchmark of the KDA hot path on GB300: chunked prefill tokens/s and decode state GB/s.
+
+Default run (N=1): the prefill_8k workload (one sequence, T=8192, H=32,
+dk=dv=128, bf16 inputs, fp32 final state) through kda_chunk_fwd -- one step is
+one full chunked forward (gate, intra-chunk transform, state recurrence,
+output).  The same line carries the decode workload (256 sequences x 1 token,
+H=32, 128 consecutive in-place steps on a 512 MiB fp32 state) through
+kda_decode_step, the roofline of the dominant kernel, the end-to-end number
+with host buffers, the CPU oracle timed on the host cores, and the SM clocks
+seen during the timed region.
+
+With --impl reference the fp64 CPU oracle runs the same workload on the host
+cores (a bounded sample of tokens per step) and prints the same JSON line.
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
+workload (the (sequence, head) units are independent; no collective is on the
+data path), so `value` is weak-scaling aggregate throughput = N x per-replica
+work / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s and decode state GB/s per GB300; % of roofline"
+PREFILL = "prefill_8k"
+DECODE = "decode_256"
+L2_BYTES = 129 * 1024 * 1024
+FLUSH_BYTES = 256 * 1024 * 1024
+# fallbacks only when the measured peaks file is absent
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK), "fallback"
+
+
+def prefill_bytes(seqlens, H, dk, dv, elt, h0: bool, hT: bool) -> int:
+    """Algorithmic HBM bytes of one chunked forward: q, k, z, v, beta read, o written once,
+    states read/written once (intermediates are not algorithmic)."""
+    T = sum(seqlens)
+    per_tok = H * ((2 * dk + dk + dv) * elt + elt + dv * elt)
+    st = len(seqlens) * H * dk * dv * 4
+    return T * per_tok + (st if h0 else 0) + (st if hT else 0)
+
+
+def prefill_flops(seqlens, H, dk, dv) -> int:
+    """Fixed flop convention per token-head: 6 dk dv + 64 (3 dk + 2 dv)."""
+    return sum(seqlens) * H * (6 * dk * dv + 64 * (3 * dk + 2 * dv))
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def __enter__(self):
+        try:
+            self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        return False
+
+    def summary(self):
+        if self.proc is None or self.out is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows),
+                "power_w_max": max((float(r[3]) for r in rows
+                                    if r[3].replace(".", "").isdigit()), default=None)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate(per_rank_units: float, elapsed_s: float, world: int) -> tuple[float, float]:
+    """(whole-job throughput, max-over-ranks seconds) for weak scaling."""
+    tmax = max_over_ranks(elapsed_s, world)
+    return per_rank_units * world / tmax, tmax
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from gated_delta_rule_43_gb300 import _build, inputs, kda
+
+    _build.build()
+    kda.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk, pk_src = peaks()
+    w = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_workload(w, device=dev)
+    T = sum(d["seqlens"])
+    N = len(d["seqlens"])
+    H, dk, dv = w.H, w.dk, w.dv
+    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, N, H, dk, dv, d["q"].dtype), dev)
+    o = torch.empty(T, H, dv, dtype=d["q"].dtype, device=dev)
+    hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def step():
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
+                      d["h0"], o=o, final_state=hT, workspace=ws, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    kda.query_status(ws, stream, raise_on_error=True)
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        for i in range(K):
+            flush.zero_()                       # evict L2 between timed steps
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    kda.query_status(ws, stream, raise_on_error=True)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    elapsed = sum(step_ms) / 1e3
+    value, tmax = aggregate(T * K, elapsed, world)
+    launches_per_step = 1
+    algo_bytes = prefill_bytes(d["seqlens"], H, dk, dv, 2, d["h0"] is not None, True)
+    kern_s = statistics.mean(step_ms) / 1e3
+    achieved_gbs = algo_bytes / kern_s / 1e9
+    flops = prefill_flops(d["seqlens"], H, dk, dv)
+    tflops = flops / kern_s / 1e12
+    hbm_peak = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    tc_peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": tmax * 1e3 / K, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{PREFILL}: B=1, H=32, T=8192, dk=dv=128, bf16 q/k/v/z/beta, "
+                               "zero initial state, fp32 final state emitted",
+                   "tokens_per_step": T, "heads": H, "dk": dk, "dv": dv,
+                   "l2": "flushed between timed steps (256 MiB write outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved_gbs / hbm_peak, "traffic": None,
+                     "kernel": "chunk_fwd_simt_kernel", "peak_source": pk_src,
+                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "tensor": {"achieved_tflops": tflops, "peak_tflops": tc_peak,
+                                "frac": tflops / tc_peak, "flops_per_launch": flops}},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk.summary(),
+    }
+    if not args.no_decode:
+        line["decode"] = decode_bench(args, dev, stream, world, pk, pk_src)
+    if not args.no_e2e:
+        line["e2e"] = e2e_bench(args, d, dev, stream, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(d, args)
+    return line
+
+
+def decode_bench(args, dev, stream, world, pk, pk_src):
+    import torch
+
+    from gated_delta_rule_43_gb300 import inputs, kda
+
+    w = inputs.WORKLOADS[DECODE]
+    ds = inputs.decode_workload(w, device=dev)
+    S = ds.state0
+    steps = args.decode_steps
+    xs = [ds.step() for _ in range(min(steps, 8))]  # fresh inputs cycle (inputs are 10 MB)
+    o = torch.empty(w.N, w.H, w.dv, dtype=torch.bfloat16, device=dev)
+    ws = kda.alloc_workspace(kda.load().kda_decode_workspace_size(), dev)
+
+    def step(i):
+        x = xs[i % len(xs)]
+        kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, S, o=o,
+                        workspace=ws, stream=stream)
+
+    for i in range(3):
+        step(i)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(steps + 1)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    ev[0].record(stream)
+    for i in range(steps):
+        step(i)
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(steps)]
+    med = statistics.median(per) / 1e3
+    state_bytes = 2 * w.N * w.H * w.dk * w.dv * 4
+    io_bytes = w.N * w.H * ((3 * w.dk + 2 * w.dv) * 2 + 2)
+    gbs_state = state_bytes / med / 1e9
+    agg, tmax = aggregate(state_bytes * steps / 1e9, sum(per) / 1e3, world)
+    hbm = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
+    achieved = (state_bytes + io_bytes) / med / 1e9
+    return {"workload": f"{DECODE}: N=256 x 1 token, H=32, dk=dv=128, bf16 q/k/v/z/beta, "
+                        "fp32 state [256,32,128,128] (512 MiB, larger than L2) in place, "
+                        f"{steps} consecutive steps",
+            "value": agg, "unit": "state GB/s", "median_step_us": med * 1e6,
+            "state_gbs_median_step": gbs_state, "steps": steps,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                         "frac": achieved / hbm, "traffic": None,
+                         "kernel": "decode_step_kernel", "peak_source": pk_src,
+                         "algorithmic_bytes_per_launch": state_bytes + io_bytes},
+            "gpu_launches": steps}
+
+
+def e2e_bench(args, d, dev, stream, world):
+    """Same prefill metric through the public call with pinned host buffers:
+    H2D of every input and D2H of o and the final state inside the timed region."""
+    import torch
+
+    from gated_delta_rule_43_gb300 import kda
+
+    names = ("q", "k", "v", "z", "beta", "A_log", "cu_seqlens")
+    host = {n: d[n].cpu().pin_memory() for n in names}
+    devb = {n: torch.empty_like(d[n]) for n in names}
+    T, H, dv = d["v"].shape
+    N = d["cu_seqlens"].numel() - 1
+    dk = d["q"].shape[2]
+    o = torch.empty(T, H, dv, dtype=d["q"].dtype, device=dev)
+    hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
+    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+    s_h = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
+    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, N, H, dk, dv, o.dtype), dev)
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o.numel() * o.element_size() + hT.numel() * 4
+
+    def step():
+        for n in names:
+            devb[n].copy_(host[n], non_blocking=True)
+        kda.chunk_fwd(devb["q"], devb["k"], devb["v"], devb["z"], devb["beta"], devb["A_log"],
+                      devb["cu_seqlens"], None, o=o, final_state=hT, workspace=ws,
+                      stream=stream)
+        o_h.copy_(o, non_blocking=True)
+        s_h.copy_(hT, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    K = max(3, args.steps // 2)
+    barrier(world)
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record(stream)
+    for _ in range(K):
+        step()
+    e.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    val, _ = aggregate(T * K, s.elapsed_time(e) / 1e3, world)
+    return {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": K}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_rate(d, target_s: float, nthreads: int = 0):
+    """Time the fp64 oracle on a prefix sample of the prefill workload sized to ~target_s.
+
+    Returns (tokens/s, sample description, threads)."""
+    import numpy as np
+
+    from gated_delta_rule_43_gb300 import inputs
+    from oracle import oracle as orc
+
+    T = sum(d["seqlens"])
+    arrs = {n: inputs.host_array(d[n]) for n in ("q", "k", "v", "z", "beta")}
+    A = d["A_log"].cpu().numpy().astype(np.float64)
+
+    def run(t):
+        t0 = time.perf_counter()
+        orc.forward(arrs["q"][:t], arrs["k"][:t], arrs["v"][:t], arrs["z"][:t],
+                    arrs["beta"][:t], A, [0, t], None, want_o=True, want_state=True,
+                    nthreads=nthreads)
+        return time.perf_counter() - t0
+
+    probe = min(T, 128)
+    dt = run(probe)
+    t_s = int(min(T, max(probe, probe * target_s / max(dt, 1e-6))))
+    dt = run(t_s)
+    return t_s / dt, t_s, orc.threads() if nthreads <= 0 else nthreads
+
+
+def cpu_baseline(d, args):
+    rate, t_s, thr = oracle_sample_rate(d, args.cpu_seconds)
+    T = sum(d["seqlens"])
+    return {"value": rate, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+            "sample": f"first {t_s} of {T} tokens of {PREFILL}, all 32 heads, fp64 sequential "
+                      f"recurrence (C, OpenMP over head x column-block units)"}
+
+
+def run_reference(args, rank, world):
+    """--impl reference: the fp64 oracle on the host cores, bounded sample per step."""
+    import torch
+
+    from gated_delta_rule_43_gb300 import inputs
+
+    if rank != 0:
+        return None
+    w = inputs.WORKLOADS[PREFILL]
+    d = inputs.make_workload(w, device="cpu")
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    rate, t_s, thr = oracle_sample_rate(d, per_step)
+    rates = []
+    for _ in range(args.warmup):
+        oracle_sample_rate(d, per_step)
+    for _ in range(args.steps):
+        r, t_s, thr = oracle_sample_rate(d, per_step)
+        rates.append(r)
+    value = statistics.mean(rates)
+    T = sum(d["seqlens"])
+    sample = (f"first {t_s} of {T} tokens of {PREFILL} per step, all 32 heads, fp64 "
+              "sequential recurrence on the host cores")
+    del torch
+    return {"metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": t_s / value * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{PREFILL}: B=1, H=32, T=8192, dk=dv=128, bf16 inputs "
+                                   "widened to fp64", "parallelism": "host cores"},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--decode-steps", type=int, default=128)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", str(args.gpus)))
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return 0
+    rank, world, local = dist_setup()
+    line = run_ours(args, rank, world, local)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

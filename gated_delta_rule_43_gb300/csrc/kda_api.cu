@@ -1,0 +1,182 @@
+// kda_api.cu -- the C ABI of libkda.so (declared in include/kda.h): argument
+// validation, workspace layout and kernel dispatch.  No device memory is
+// allocated here; every buffer comes from the caller.
+#include <stdint.h>
+#include <string.h>
+
+#include "kda_common.cuh"
+
+namespace kda {
+cudaError_t launch_decode(int dtype, int dk, int dv, const void *q, const void *k,
+                          const void *v, const void *z, const void *beta, const float *A_log,
+                          float *state, void *o, int N, int H, cudaStream_t s);
+cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const void *k,
+                              const void *v, const void *z, const void *beta,
+                              const float *A_log, const int32_t *cu, int N, int64_t T_tot, int H,
+                              const float *h0, float *hT, void *o, StatusWord *st,
+                              cudaStream_t s);
+cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
+                        StatusWord *st, cudaStream_t s);
+cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
+                        const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
+                        float *G, StatusWord *st, cudaStream_t s);
+}  // namespace kda
+
+using namespace kda;
+
+namespace {
+
+constexpr int32_t kAbiVersion = 1;
+
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
+inline bool head_ok(int32_t d) { return d == 32 || d == 64 || d == 128; }
+
+struct ChunkLayout {
+    size_t plan_off, plan_bytes, total;
+};
+
+ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv) {
+    (void)T; (void)H; (void)dk; (void)dv;
+    ChunkLayout L;
+    L.plan_off = kHeaderBytes;
+    L.plan_bytes = round_up(sizeof(int32_t) * ((size_t)N + 1), 256);
+    L.total = L.plan_off + L.plan_bytes;
+    return L;
+}
+
+kda_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
+
+// Grids over chunk slots use gridDim.x, which is limited to 2^31 - 1.
+bool chunk_slots_overflow(int64_t T, int32_t N, int32_t C) {
+    return (T + C - 1) / C + N > 0x7fffffffLL;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t kda_abi_version(void) { return kAbiVersion; }
+
+const char *kda_status_string(int32_t s) {
+    switch (s) {
+        case KDA_OK: return "KDA_OK";
+        case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+        case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported head size or dtype";
+        case KDA_ERR_DECAY_RANGE:
+            return "KDA_ERR_DECAY_RANGE: 16-token cumulative log-decay not finite or outside [-80, 0]";
+        case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device wait expired";
+        case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime error";
+        case KDA_ERR_SEQLENS: return "KDA_ERR_SEQLENS: inconsistent cu_seqlens";
+        default: return "KDA_ERR_UNKNOWN";
+    }
+}
+
+size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
+                                    int32_t dk, int32_t dv, int32_t dtype) {
+    if (total_tokens < 0 || num_seqs < 0 || H <= 0 || !head_ok(dk) || !head_ok(dv) ||
+        (dtype != KDA_F32 && dtype != KDA_BF16))
+        return 0;
+    return chunk_layout(total_tokens, num_seqs, H, dk, dv).total;
+}
+
+size_t kda_decode_workspace_size(void) { return kHeaderBytes; }
+
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *z,
+                         const void *beta, const float *A_log, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                         int32_t dv, int32_t dtype, const float *initial_state,
+                         float *final_state, void *o, void *workspace, size_t workspace_bytes,
+                         void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > ((int64_t)1 << 40) / ((int64_t)H * (dk > dv ? dk : dv)))
+        return KDA_ERR_INVALID_ARG;
+    if (!A_log || !cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, z, o, initial_state, final_state};
+    for (const void *p : al16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
+    if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
+    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dv);
+    if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    StatusWord *st = (StatusWord *)workspace;
+    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
+    e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
+                          total_tokens, H, initial_state, final_state, o, st, s);
+    return cuda_status(e);
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                           const void *beta, const float *A_log, float *state, void *o,
+                           int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)N * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < kHeaderBytes || !aligned(workspace, 256))
+        return KDA_ERR_INVALID_ARG;
+    if (N > 0 && (!q || !k || !v || !z || !beta || !A_log || !state || !o))
+        return KDA_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, z, o, state};
+    for (const void *p : al16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (o && (o == q || o == k || o == v || o == z || o == beta || o == (void *)state))
+        return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(StatusWord), s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (N == 0) return KDA_OK;
+    return cuda_status(launch_decode(dtype, dk, dv, q, k, v, z, beta, A_log, state, o, N, H, s));
+}
+
+kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_seqlens,
+                           int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                           int32_t dtype, int32_t chunk, float *g_cumsum, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_ok(dk)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0 || chunk <= 0 || chunk % kTile != 0)
+        return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (!A_log || !cu_seqlens || !workspace || (total_tokens > 0 && (!z || !g_cumsum)))
+        return KDA_ERR_INVALID_ARG;
+    if (!aligned(z, 16) || !aligned(g_cumsum, 16) || !aligned(workspace, 256))
+        return KDA_ERR_INVALID_ARG;
+    if ((const void *)g_cumsum == z && g_cumsum) return KDA_ERR_INVALID_ARG;
+    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dk);
+    if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
+    if (chunk_slots_overflow(total_tokens, num_seqs, chunk)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    StatusWord *st = (StatusWord *)workspace;
+    int32_t *chunk_off = (int32_t *)((char *)workspace + L.plan_off);
+    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
+    e = launch_plan(cu_seqlens, num_seqs, total_tokens, chunk, chunk_off, st, s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    e = launch_gate(dtype, z, A_log, cu_seqlens, chunk_off, num_seqs, total_tokens, H, dk, chunk,
+                    g_cumsum, st, s);
+    return cuda_status(e);
+}
+
+kda_status kda_query_status(const void *workspace, void *stream, int64_t *info) {
+    if (!workspace) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    StatusWord w;
+    if (cudaMemcpy(&w, workspace, sizeof w, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (info) *info = (int64_t)w.info;
+    return (kda_status)w.code;
+}
+
+}  // extern "C"

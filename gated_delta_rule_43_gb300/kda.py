@@ -1,0 +1,193 @@
+"""Thin Python binding of libkda.so (the C ABI in include/kda.h).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI.  PyTorch supplies device memory and the stream.
+There is no CPU fallback: if the library is missing or no GPU is present the
+calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_DECAY_RANGE = 0, 1, 2, 3
+KDA_ERR_TIMEOUT, KDA_ERR_CUDA, KDA_ERR_SEQLENS = 4, 5, 6
+KDA_F32, KDA_BF16 = 0, 1
+_DT = {torch.float32: KDA_F32, torch.bfloat16: KDA_BF16}
+
+# name -> (restype, argtypes) of every symbol include/kda.h declares
+P, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+SIGNATURES = {
+    "kda_abi_version": (I32, []),
+    "kda_status_string": (ctypes.c_char_p, [I32]),
+    "kda_chunk_fwd_workspace_size": (SZ, [I64, I32, I32, I32, I32, I32]),
+    "kda_chunk_fwd": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, P, SZ,
+                            P]),
+    "kda_decode_workspace_size": (SZ, []),
+    "kda_decode_step": (I32, [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P]),
+    "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, P, P, SZ, P]),
+    "kda_query_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int64)]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, code: int, where: str, info: int | None = None):
+        self.code = code
+        self.info = info
+        msg = f"{where}: {status_string(code)}"
+        if info is not None:
+            msg += f" (info={info})"
+        super().__init__(msg)
+
+
+def load(path: str = LIB_PATH):
+    """Load libkda.so (once).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"{path} is missing: build it with `python -c 'import __graft_entry__ as g; "
+                    "g.build()'` (there is no CPU fallback)")
+            lib = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().kda_status_string(int(code)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None:
+            if not t.is_cuda:
+                raise ValueError("every tensor must live on a CUDA device (no CPU fallback)")
+            if not t.is_contiguous():
+                raise ValueError("tensors must be contiguous")
+
+
+def chunk_fwd_workspace_size(total_tokens: int, num_seqs: int, H: int, dk: int, dv: int,
+                             dtype: torch.dtype) -> int:
+    return int(load().kda_chunk_fwd_workspace_size(total_tokens, num_seqs, H, dk, dv,
+                                                   _DT[dtype]))
+
+
+def alloc_workspace(nbytes: int, device) -> torch.Tensor:
+    # torch's caching allocator returns 512-byte aligned blocks
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
+def chunk_fwd(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None, *,
+              output_final_state: bool = True, o=None, final_state=None, workspace=None,
+              stream=None, check: bool = False):
+    """KDA chunked prefill over packed sequences (kda_chunk_fwd).
+
+    q, k, z [T, H, dk], v [T, H, dv], beta [T, H] (fp32 or bf16, one dtype);
+    A_log [H] fp32; cu_seqlens [N+1] int32; initial_state [N, H, dk, dv] fp32
+    or None.  Returns (o [T, H, dv], final_state [N, H, dk, dv] fp32 or None).
+    ``final_state`` may be passed as ``initial_state`` for an in-place update.
+    With ``check=True`` the stream is synchronised and a device-side error
+    raises KdaError.
+    """
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dt = _DT[q.dtype]
+    if A_log.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("A_log must be fp32 and cu_seqlens int32")
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    need = int(lib.kda_chunk_fwd_workspace_size(T, N, H, dk, dv, dt))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    rc = lib.kda_chunk_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),
+                           _ptr(cu_seqlens), N, T, H, dk, dv, dt, _ptr(initial_state),
+                           _ptr(final_state), _ptr(o), _ptr(workspace), workspace.numel(),
+                           _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd")
+    if check:
+        query_status(workspace, stream, raise_on_error=True)
+    return o, final_state
+
+
+def decode_step(q, k, v, z, beta, A_log, state, *, o=None, workspace=None, stream=None):
+    """One decode step for N sequences (kda_decode_step); `state` is updated in place.
+
+    q, k, z [N, H, dk], v [N, H, dv], beta [N, H]; state [N, H, dk, dv] fp32.
+    Returns o [N, H, dv].
+    """
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, state, o, workspace)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state.dtype != torch.float32:
+        raise TypeError("state must be fp32")
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(int(lib.kda_decode_workspace_size()), q.device)
+    rc = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),
+                             _ptr(state), _ptr(o), N, H, dk, dv, _DT[q.dtype], _ptr(workspace),
+                             workspace.numel(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step")
+    return o
+
+
+def gate_cumsum(z, A_log, cu_seqlens, chunk: int = 64, *, workspace=None, stream=None,
+                check: bool = False):
+    """The standalone gate kernel (kda_gate_cumsum): fp32 in-chunk cumsum of g [T, H, dk]."""
+    lib = load()
+    _check_cuda(z, A_log, cu_seqlens, workspace)
+    T, H, dk = z.shape
+    N = cu_seqlens.numel() - 1
+    G = torch.empty(T, H, dk, dtype=torch.float32, device=z.device)
+    dt = _DT[z.dtype]
+    if workspace is None:
+        workspace = alloc_workspace(int(lib.kda_chunk_fwd_workspace_size(T, N, H, dk, dk, dt)),
+                                    z.device)
+    rc = lib.kda_gate_cumsum(_ptr(z), _ptr(A_log), _ptr(cu_seqlens), N, T, H, dk, dt, chunk,
+                             _ptr(G), _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_gate_cumsum")
+    if check:
+        query_status(workspace, stream, raise_on_error=True)
+    return G, workspace
+
+
+def query_status(workspace, stream=None, *, raise_on_error: bool = False):
+    """(code, info) recorded in `workspace` by the last call (synchronises the stream)."""
+    info = ctypes.c_int64(0)
+    rc = load().kda_query_status(_ptr(workspace), _stream(stream), ctypes.byref(info))
+    if raise_on_error and rc != KDA_OK:
+        raise KdaError(rc, "device status", info.value)
+    return rc, info.value

@@ -1,0 +1,161 @@
+/*
+ * kda.h -- C ABI of libkda.so: Kimi Delta Attention (KDA) on one GB300 (sm_103a).
+ *
+ * The operation (per head h of every sequence) is defined on the dev.to page
+ * "Kimi K3 Architecture: Scaling 2.8T Parameters for Long-Context Multimodal
+ * MoE", section "The Sequence Bottleneck: Hybrid KDA and Gated MLA":
+ *   gate   g_t = g_min * Sigmoid(exp(A_h) * z_t),  g_min = -5,  alpha_t = exp(g_t)
+ *   state  S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *   output o_t = S_t^T q_t
+ * with a fixed-size dk x dv fp32 state per (sequence, head) (also "Kimi K3 -
+ * Sparsity Mechanics...", section 2, "Temporal Sequence (KDA)").  The same
+ * section of the dev.to page bounds the cumulative log-decay of every 16-token
+ * tile to (-80, 0), which is what lets the chunked form run on bf16 tiles.
+ *
+ * Conventions shared by every entry point
+ *  - Layout "THD": token-major packed tensors [T_tot, H, D], D contiguous.
+ *    q, k, z: D = dk; v and o: D = dv; beta: [T_tot, H].
+ *  - States are fp32 [N, H, dk, dv], row-major: S[n][h][i][j], i the key
+ *    channel (dk), j the value channel (dv).
+ *  - dtype selects the storage type of q, k, v, z, beta and o: KDA_F32 or
+ *    KDA_BF16.  A_log ([H], the per-head A^h) and all states are fp32.
+ *    Arithmetic is fp32 (bf16 tensor-core operands where a kernel says so).
+ *  - q must arrive already normalised and scaled; the library applies no
+ *    scale and no normalisation.  beta must already lie in (0, 1).
+ *  - Every pointer except `stream` is a DEVICE pointer.  The caller owns and
+ *    allocates every buffer, including the workspace; the library allocates
+ *    no device memory and keeps no per-call state.
+ *  - Pointers to q, k, v, z, o and states must be 16-byte aligned.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL means
+ *    the legacy default stream).  Argument errors are returned synchronously
+ *    and nothing is launched.  Errors found on the device (a non-finite or
+ *    out-of-range cumulative decay, inconsistent cu_seqlens, a bounded wait
+ *    that expired) are recorded in a status word at the start of the
+ *    workspace; read it with kda_query_status.  The first error recorded wins.
+ *  - Supported head sizes: dk, dv in {32, 64, 128}.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kda_status {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, aliasing, small workspace */
+    KDA_ERR_UNSUPPORTED = 2, /* head size or dtype this library does not build */
+    KDA_ERR_DECAY_RANGE = 3, /* a 16-token cumulative log-decay not finite or outside [-80, 0] */
+    KDA_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired */
+    KDA_ERR_CUDA = 5,        /* a CUDA runtime call failed */
+    KDA_ERR_SEQLENS = 6      /* cu_seqlens not 0-based, decreasing, or not ending at T_tot */
+} kda_status;
+
+typedef enum kda_dtype { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Version of this ABI (bumped on any signature change). */
+int32_t kda_abi_version(void);
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char *kda_status_string(int32_t status);
+
+/*
+ * Bytes of workspace kda_chunk_fwd needs for this problem size.  The
+ * workspace holds the status word, the chunk plan of the packed sequences
+ * and the intermediates of the chunked form; its contents need no
+ * initialisation and are overwritten by every call.  Returns 0 for
+ * arguments kda_chunk_fwd would reject.
+ */
+size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
+                                    int32_t dk, int32_t dv, int32_t dtype);
+
+/*
+ * Chunked prefill over packed variable-length sequences.
+ *
+ * Computes, for every sequence n = 0..num_seqs-1 (tokens cu_seqlens[n] ..
+ * cu_seqlens[n+1]-1) and head h, the recurrence in the file header starting
+ * from initial_state[n][h] (zeros when initial_state is NULL); writes o for
+ * every token and, when final_state is not NULL, the state after the
+ * sequence's last token.  An empty sequence leaves its state unchanged.
+ * Internally the sequence is cut into chunks that start at the sequence's
+ * first token; the intra-chunk part runs as dense products over 16-token
+ * tiles (the chunkwise-parallel form of the dev.to page, section "The
+ * Sequence Bottleneck").  The result equals the token-by-token recurrence
+ * up to rounding.
+ *
+ *   q, k, z       [total_tokens, H, dk]  dtype
+ *   v             [total_tokens, H, dv]  dtype
+ *   beta          [total_tokens, H]      dtype
+ *   A_log         [H]                    fp32
+ *   cu_seqlens    [num_seqs + 1]         int32, device; 0 = cu[0] <= ... <= cu[num_seqs] = total_tokens
+ *   initial_state [num_seqs, H, dk, dv]  fp32 or NULL
+ *   final_state   [num_seqs, H, dk, dv]  fp32 or NULL; may alias initial_state (in-place update)
+ *   o             [total_tokens, H, dv]  dtype; must not alias any input
+ *   workspace     >= kda_chunk_fwd_workspace_size(...) bytes, 256-byte aligned
+ * Device-found errors: KDA_ERR_SEQLENS (nothing computed for the offending
+ * sequence), KDA_ERR_DECAY_RANGE (outputs of that chunk are not meaningful),
+ * KDA_ERR_TIMEOUT.
+ */
+kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *z,
+                         const void *beta, const float *A_log, const int32_t *cu_seqlens,
+                         int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                         int32_t dv, int32_t dtype, const float *initial_state,
+                         float *final_state, void *o, void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Bytes of workspace kda_decode_step needs (the status word only). */
+size_t kda_decode_workspace_size(void);
+
+/*
+ * One decode step: every one of N sequences advances by exactly one token
+ * against its resident state, which is updated in place (the constant-size
+ * state of "Kimi K3 - Sparsity Mechanics...", section 2 "Temporal Sequence
+ * (KDA)", "constant decoding memory"; the update of the dev.to page).
+ *
+ *   q, k, z  [N, H, dk]  dtype       v  [N, H, dv]  dtype      beta [N, H] dtype
+ *   A_log    [H] fp32
+ *   state    [N, H, dk, dv] fp32, read and written in place
+ *   o        [N, H, dv]  dtype
+ *   workspace >= kda_decode_workspace_size() bytes
+ * The state is streamed once from HBM and written once; the step is
+ * memory-bound.  Device-found errors: none beyond KDA_ERR_CUDA (a non-finite
+ * gate propagates into the state and output as in the definition).
+ */
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                           const void *beta, const float *A_log, float *state, void *o,
+                           int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                           void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * The gate on its own: g = -5 Sigmoid(exp(A_h) z) per channel and its
+ * inclusive cumulative sum restarted every `chunk` tokens (chunks start at
+ * each sequence's first token), written as fp32 [total_tokens, H, dk].
+ * Also range-checks every 16-token tile prefix sum against [-80, 0]
+ * (dev.to page, section "The Sequence Bottleneck", the bound after the gate
+ * equation) and records KDA_ERR_DECAY_RANGE on a violation.  `chunk` must
+ * be a positive multiple of 16.  kda_chunk_fwd fuses the same computation
+ * into its own kernels; this entry exposes it for inspection.
+ * Workspace: >= kda_chunk_fwd_workspace_size(total_tokens, num_seqs, H, dk, dk, dtype).
+ */
+kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_seqlens,
+                           int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                           int32_t dtype, int32_t chunk, float *g_cumsum, void *workspace,
+                           size_t workspace_bytes, void *stream);
+
+/*
+ * Waits for `stream`, then returns the status recorded in `workspace` by the
+ * last call that used it (KDA_OK if none).  When `info` is not NULL it
+ * receives a detail of the first error: the flat token*H+head index of a
+ * decay-range violation, the sequence index of a cu_seqlens error, or the
+ * site of an expired wait.
+ */
+kda_status kda_query_status(const void *workspace, void *stream, int64_t *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

@@ -1,0 +1,77 @@
+"""Shared helpers of the GPU parity tests: run the CUDA path, run the oracle, score."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from gated_delta_rule_43_gb300 import inputs, kda
+from oracle import oracle as orc
+
+# Relative L2 tolerances: fp32 storage 1e-4, bf16 storage 1e-2 (outputs and final states).
+TOL = {"f32": 1e-4, "bf16": 1e-2}
+DTYPE_NAME = {torch.float32: "f32", torch.bfloat16: "bf16"}
+
+
+def rel_l2(x, ref) -> float:
+    return orc.rel_l2(x, ref)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def gpu_prefill(d, *, final=True, check=True):
+    return kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
+                         d["h0"], output_final_state=final, check=check)
+
+
+def host_inputs(d, seqs=None, heads=None):
+    """Host arrays (exact storage precision) of a packed input dict, optionally sub-sampled.
+
+    seqs: indices of sequences to keep (re-packed); heads: indices of heads to keep.
+    Returns (arrays dict, A_log fp64, cu int64, h0 fp64 or None, token index array).
+    """
+    cu = d["cu_seqlens"].cpu().numpy().astype(np.int64)
+    N = len(cu) - 1
+    seqs = list(range(N)) if seqs is None else list(seqs)
+    tok = np.concatenate([np.arange(cu[n], cu[n + 1]) for n in seqs]) if seqs else np.zeros(0,
+                                                                                           int)
+    lens = [int(cu[n + 1] - cu[n]) for n in seqs]
+    cu_sub = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    H = d["q"].shape[1]
+    hsel = list(range(H)) if heads is None else list(heads)
+    tok_t = torch.as_tensor(tok, device=d["q"].device, dtype=torch.long)
+    hs_t = torch.as_tensor(hsel, device=d["q"].device, dtype=torch.long)
+    arrs = {}
+    for name in ("q", "k", "v", "z", "beta"):
+        t = d[name].index_select(0, tok_t).index_select(1, hs_t)
+        arrs[name] = inputs.host_array(t)
+    A = d["A_log"].index_select(0, hs_t.to(d["A_log"].device)).cpu().numpy().astype(np.float64)
+    h0 = None
+    if d["h0"] is not None:
+        sel = torch.as_tensor(seqs, device=d["h0"].device, dtype=torch.long)
+        h0 = d["h0"].index_select(0, sel).index_select(1, hs_t).cpu().numpy().astype(np.float64)
+    return arrs, A, cu_sub, h0, tok, hsel
+
+
+def oracle_prefill(d, seqs=None, heads=None, o_cmp=None):
+    arrs, A, cu, h0, tok, hsel = host_inputs(d, seqs, heads)
+    return orc.forward(arrs["q"], arrs["k"], arrs["v"], arrs["z"], arrs["beta"], A, cu, h0,
+                       o_cmp=o_cmp), tok, hsel
+
+
+def score_prefill(d, o, hT, seqs=None, heads=None):
+    """(rel-L2 of o, rel-L2 of the final state) against the oracle on the selected slice."""
+    ref, tok, hsel = oracle_prefill(d, seqs, heads)
+    dev = o.device
+    o_sel = o.index_select(0, torch.as_tensor(tok, device=dev, dtype=torch.long)).index_select(
+        1, torch.as_tensor(hsel, device=dev, dtype=torch.long))
+    e_o = rel_l2(to_f64(o_sel), ref["o"])
+    e_s = None
+    if hT is not None:
+        N = d["cu_seqlens"].numel() - 1
+        seqs = list(range(N)) if seqs is None else list(seqs)
+        s_sel = hT.index_select(0, torch.as_tensor(seqs, device=dev, dtype=torch.long))
+        s_sel = s_sel.index_select(1, torch.as_tensor(hsel, device=dev, dtype=torch.long))
+        e_s = rel_l2(to_f64(s_sel), ref["state"])
+    return e_o, e_s

@@ -1,0 +1,81 @@
+"""GPU parity of kda_decode_step against the fp64 oracle (called through the C ABI)."""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_43_gb300 import inputs, kda
+from oracle import oracle as orc
+from tests.gpu_util import TOL, gpu_prefill, rel_l2, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _decode_and_score(N, H, dk, dv, dtype, steps, seqs=None, seed=0):
+    ds = inputs.DecodeStream(N, H, dk, dv, dtype, seed=seed, h0_sigma=0.1, device=DEV)
+    state = ds.state0.clone()
+    sel = list(range(N)) if seqs is None else list(seqs)
+    sel_t = torch.as_tensor(sel, device=DEV)
+    ref_state = state.index_select(0, sel_t).cpu().numpy().astype(np.float64)
+    A = ds.A_log.cpu().numpy().astype(np.float64)
+    outs, refs = [], []
+    for _ in range(steps):
+        x = ds.step()
+        o = kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, state)
+        outs.append(to_f64(o.index_select(0, sel_t)))
+        h = {k: inputs.host_array(x[k].index_select(0, sel_t)) for k in x}
+        refs.append(orc.decode(h["q"], h["k"], h["v"], h["z"], h["beta"], A, ref_state))
+    torch.cuda.synchronize()
+    e_o = rel_l2(np.stack(outs), np.stack(refs))
+    e_s = rel_l2(to_f64(state.index_select(0, sel_t)), ref_state)
+    tol = TOL[dtype]
+    assert e_o <= tol, f"decode o rel-L2 {e_o:.3e} > {tol}"
+    assert e_s <= tol, f"decode state rel-L2 {e_s:.3e} > {tol}"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", [(32, 32), (32, 128), (64, 64), (128, 32), (128, 128)])
+def test_decode_small(dtype, dk, dv):
+    _decode_and_score(5, 3, dk, dv, dtype, steps=6, seed=dk + dv)
+
+
+def test_decode_256_workload_sampled():
+    """256 sequences, H=32, 128 steps in place; 16 sequences scored over every step."""
+    g = torch.Generator().manual_seed(30)
+    seqs = sorted(torch.randperm(256, generator=g)[:16].tolist())
+    _decode_and_score(256, 32, 128, 128, "bf16", steps=128, seqs=seqs, seed=3)
+
+
+def test_tiny_workload_as_decode_steps():
+    """The tiny fp32 workload run as 64 decode steps equals its 64-token prefill."""
+    d = inputs.make_workload(inputs.WORKLOADS["tiny_fp32"], device=DEV)
+    o_pre, s_pre = gpu_prefill(d)
+    H, dk, dv = 2, 32, 32
+    state = torch.zeros(1, H, dk, dv, device=DEV)
+    outs = []
+    for t in range(64):
+        sl = slice(t, t + 1)
+        outs.append(kda.decode_step(d["q"][sl], d["k"][sl], d["v"][sl], d["z"][sl],
+                                    d["beta"][sl], d["A_log"], state))
+    o_dec = torch.cat(outs)
+    assert rel_l2(to_f64(o_dec), to_f64(o_pre)) <= TOL["f32"]
+    assert rel_l2(to_f64(state), to_f64(s_pre)) <= TOL["f32"]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_prefill_then_decode_handoff(dtype):
+    """Prefill 50 tokens, then decode 10 more from the emitted state = one 60-token pass."""
+    d = inputs.make_prefill([60], H=2, dk=128, dv=128, dtype=dtype, seed=5, h0_sigma=0.1,
+                            device=DEV)
+    o_all, s_all = gpu_prefill(d)
+    a = {k: (v[:50] if k in ("q", "k", "v", "z", "beta") else v) for k, v in d.items()}
+    a["cu_seqlens"] = torch.tensor([0, 50], dtype=torch.int32, device=DEV)
+    o_a, S = gpu_prefill(a)
+    outs = [o_a]
+    for t in range(50, 60):
+        sl = slice(t, t + 1)
+        outs.append(kda.decode_step(d["q"][sl], d["k"][sl], d["v"][sl], d["z"][sl],
+                                    d["beta"][sl], d["A_log"], S))
+    tol = TOL[dtype]
+    assert rel_l2(to_f64(torch.cat(outs)), to_f64(o_all)) <= tol
+    assert rel_l2(to_f64(S), to_f64(s_all)) <= tol

@@ -1,0 +1,54 @@
+"""The standalone gate kernel and device-side error reporting (GPU).
+
+Errors are provoked with bad INPUT values (NaN in z, inconsistent
+cu_seqlens) that the kernels check themselves; nothing here faults a GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+from gated_delta_rule_43_gb300 import inputs, kda
+from oracle import oracle as orc
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("chunk", [16, 64])
+def test_gate_cumsum_matches_oracle(dtype, chunk):
+    d = inputs.make_prefill([100, 0, 33, 64], H=3, dk=64, dv=32, dtype=dtype, seed=9,
+                            device=DEV)
+    G, ws = kda.gate_cumsum(d["z"], d["A_log"], d["cu_seqlens"], chunk=chunk, check=True)
+    _, Gref, bad = orc.gate(inputs.host_array(d["z"]), d["A_log"].cpu().numpy(),
+                            d["cu_seqlens"].cpu().numpy(), tile=chunk)
+    assert bad == 0 or chunk > 16
+    err = np.abs(G.cpu().numpy().astype(np.float64) - Gref)
+    assert float(err.max()) <= 1e-5 * max(1.0, float(np.abs(Gref).max()))
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_nan_decay_is_reported(dtype):
+    d = inputs.make_prefill([40, 40], H=2, dk=32, dv=32, dtype=dtype, seed=1, device=DEV)
+    d["z"][45, 1, 3] = float("nan")
+    with pytest.raises(kda.KdaError) as ei:
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
+                      check=True)
+    assert ei.value.code == kda.KDA_ERR_DECAY_RANGE
+    assert ei.value.info == 45 * 2 + 1
+    with pytest.raises(kda.KdaError) as eg:
+        kda.gate_cumsum(d["z"], d["A_log"], d["cu_seqlens"], chunk=64, check=True)
+    assert eg.value.code == kda.KDA_ERR_DECAY_RANGE
+
+
+def test_bad_cu_seqlens_are_reported():
+    d = inputs.make_prefill([10, 10, 10], H=1, dk=32, dv=32, dtype="f32", seed=2, device=DEV)
+    for bad in ([0, 10, 5, 30], [0, 10, 20, 25], [1, 10, 20, 30]):
+        cu = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        with pytest.raises(kda.KdaError) as ei:
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], cu, check=True)
+        assert ei.value.code == kda.KDA_ERR_SEQLENS
+    # the status word is cleared by the next good call
+    o, s = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                         d["cu_seqlens"], check=True)
+    assert torch.isfinite(o).all()

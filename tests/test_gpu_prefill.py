@@ -1,0 +1,96 @@
+"""GPU parity of kda_chunk_fwd against the fp64 oracle (called through the C ABI)."""
+import pytest
+import torch
+
+from gated_delta_rule_43_gb300 import inputs, kda
+from tests.gpu_util import TOL, gpu_prefill, rel_l2, score_prefill, to_f64
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+def _run_and_score(d, dtype, seqs=None, heads=None, final=True):
+    o, hT = gpu_prefill(d, final=final)
+    torch.cuda.synchronize()
+    e_o, e_s = score_prefill(d, o, hT, seqs, heads)
+    tol = TOL[dtype]
+    assert e_o <= tol, f"o rel-L2 {e_o:.3e} > {tol}"
+    if final:
+        assert e_s <= tol, f"state rel-L2 {e_s:.3e} > {tol}"
+    return e_o, e_s
+
+
+def test_tiny_fp32_workload():
+    """B=1, H=2, T=64, dk=dv=32, fp32, zero initial state, seed 0: rel-L2 <= 1e-4."""
+    w = inputs.WORKLOADS["tiny_fp32"]
+    d = inputs.make_workload(w, device=DEV)
+    _run_and_score(d, "f32")
+
+
+SHAPES = [(32, 32), (64, 128), (128, 64), (128, 128)]
+LENS = [[1], [15], [16], [17], [33], [100, 0, 37], [0], [64, 64, 1, 129]]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dk,dv", SHAPES)
+@pytest.mark.parametrize("lens", LENS, ids=lambda l: "-".join(map(str, l)))
+def test_small_shapes_and_ragged_tails(dtype, dk, dv, lens):
+    d = inputs.make_prefill(lens, H=3, dk=dk, dv=dv, dtype=dtype, seed=sum(lens) + dk + dv,
+                            h0_sigma=0.1 if len(lens) > 1 else 0.0, device=DEV)
+    _run_and_score(d, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_in_place_state_and_no_final_state(dtype):
+    d = inputs.make_prefill([40, 70], H=2, dk=64, dv=64, dtype=dtype, seed=7, h0_sigma=0.1,
+                            device=DEV)
+    ref_o, ref_s = gpu_prefill(d)
+    S = d["h0"].clone()
+    o, s_out = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                             d["cu_seqlens"], S, final_state=S, check=True)
+    assert s_out.data_ptr() == S.data_ptr()
+    assert torch.equal(o, ref_o) and torch.equal(S, ref_s)
+    o2, none = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                             d["cu_seqlens"], d["h0"], output_final_state=False, check=True)
+    assert none is None and torch.equal(o2, ref_o)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_split_and_resume(dtype):
+    """Prefill [0, t) then [t, T) from the carried state matches one pass."""
+    T = 300
+    d = inputs.make_prefill([T], H=2, dk=128, dv=128, dtype=dtype, seed=11, h0_sigma=0.1,
+                            device=DEV)
+    o_all, s_all = gpu_prefill(d)
+    for t in (1, 64, 100):
+        a = {k: (v[:t] if k in ("q", "k", "v", "z", "beta") else v) for k, v in d.items()}
+        a["cu_seqlens"] = torch.tensor([0, t], dtype=torch.int32, device=DEV)
+        oa, sa = gpu_prefill(a)
+        b = {k: (v[t:] if k in ("q", "k", "v", "z", "beta") else v) for k, v in d.items()}
+        b["cu_seqlens"] = torch.tensor([0, T - t], dtype=torch.int32, device=DEV)
+        b["h0"] = sa
+        ob, sb = gpu_prefill(b)
+        tol = TOL[dtype]
+        assert rel_l2(to_f64(torch.cat([oa, ob])), to_f64(o_all)) <= tol
+        assert rel_l2(to_f64(sb), to_f64(s_all)) <= tol
+
+
+def test_prefill_8k_workload():
+    """B=1, H=32, T=8192, dk=dv=128, bf16: full oracle comparison."""
+    d = inputs.make_workload(inputs.WORKLOADS["prefill_8k"], device=DEV)
+    _run_and_score(d, "bf16")
+
+
+def test_varlen_64_workload_sampled():
+    """64 packed sequences U[512, 4096], H=32, h0 ~ N(0, 0.01): full GPU run, 6 sequences scored."""
+    d = inputs.make_workload(inputs.WORKLOADS["varlen_64"], device=DEV)
+    g = torch.Generator().manual_seed(20)
+    seqs = sorted(torch.randperm(64, generator=g)[:6].tolist())
+    _run_and_score(d, "bf16", seqs=seqs)
+
+
+@pytest.mark.timeout(1800)
+def test_prefill_1m_workload_sampled():
+    """B=1, H=16, T=1,048,576: full GPU run, two heads scored over the whole length."""
+    d = inputs.make_workload(inputs.WORKLOADS["prefill_1m"], device=DEV)
+    _run_and_score(d, "bf16", heads=[0, 15])

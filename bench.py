@@ -67,6 +67,17 @@ def prefill_flops(seqlens, H, dk, dv) -> int:
     return sum(seqlens) * H * (6 * dk * dv + 64 * (3 * dk + 2 * dv))
 
 
+def kernel_names(n_events: int, tc_path: bool, has_init: bool) -> list[str]:
+    """Names of the kernels one kda_chunk_fwd_profiled call launched, in order."""
+    k = n_events - 1
+    if not tc_path:
+        return ["chunk_fwd_simt_kernel"] * k
+    names = ["plan_chunks_kernel"] + (["state_init_kernel"] if has_init else [])
+    while len(names) < k:
+        names += ["prep_kernel", "chain_kernel"]
+    return names[:k]
+
+
 class ClockSampler:
     """nvidia-smi clocks / throttle reasons sampled every 200 ms during a region."""
 
@@ -195,28 +206,44 @@ def run_ours(args, rank, world, local):
     kda.query_status(ws, stream, raise_on_error=True)
 
     K = args.steps
+    NEV = 256
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    kev = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(K)]
+    used = []
     barrier(world)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
         for i in range(K):
             flush.zero_()                       # evict L2 between timed steps
             starts[i].record(stream)
-            step()
+            used.append(kda.chunk_fwd_profiled(d["q"], d["k"], d["v"], d["z"], d["beta"],
+                                               d["A_log"], d["cu_seqlens"], d["h0"], o, hT, ws,
+                                               kev[i], stream=stream))
             ends[i].record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
     kda.query_status(ws, stream, raise_on_error=True)
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
     elapsed = sum(step_ms) / 1e3
     value, tmax = aggregate(T * K, elapsed, world)
-    launches_per_step = 1
+    # per-kernel times from the events recorded between launches
+    names = kernel_names(used[0], tc_path=(d["q"].dtype == torch.bfloat16 and dk == 128
+                                            and dv == 128), has_init=d["h0"] is not hT)
+    per_kernel = {}
+    for i in range(K):
+        for j, nm in enumerate(names):
+            per_kernel.setdefault(nm, []).append(kev[i][j].elapsed_time(kev[i][j + 1]))
+    totals = {nm: sum(v_) / K for nm, v_ in per_kernel.items()}       # ms per step
+    launches = {nm: names.count(nm) for nm in totals}
+    dom = max(totals, key=totals.get)
+    launches_per_step = len(names)
     algo_bytes = prefill_bytes(d["seqlens"], H, dk, dv, 2, d["h0"] is not None, True)
-    kern_s = statistics.mean(step_ms) / 1e3
-    achieved_gbs = algo_bytes / kern_s / 1e9
+    step_s = statistics.mean(step_ms) / 1e3
+    dom_s = totals[dom] / 1e3
+    achieved_gbs = algo_bytes / dom_s / 1e9           # per launch: bytes/launches / (time/launches)
     flops = prefill_flops(d["seqlens"], H, dk, dv)
-    tflops = flops / kern_s / 1e12
+    tflops = flops / step_s / 1e12
     hbm_peak = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
     tc_peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
 
@@ -231,10 +258,17 @@ def run_ours(args, rank, world, local):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak, "traffic": None,
-                     "kernel": "chunk_fwd_simt_kernel", "peak_source": pk_src,
-                     "algorithmic_bytes_per_launch": algo_bytes,
+                     "kernel": dom, "peak_source": pk_src,
+                     "algorithmic_bytes_per_launch": algo_bytes / launches[dom],
+                     "launches_per_step": launches[dom],
+                     "avg_launch_us": dom_s / launches[dom] * 1e6,
+                     "kernel_ms_per_step": totals,
+                     "step": {"achieved_gbs": algo_bytes / step_s / 1e9,
+                              "frac": algo_bytes / step_s / 1e9 / hbm_peak,
+                              "algorithmic_bytes": algo_bytes},
                      "tensor": {"achieved_tflops": tflops, "peak_tflops": tc_peak,
-                                "frac": tflops / tc_peak, "flops_per_launch": flops}},
+                                "frac": tflops / tc_peak, "flops_per_step": flops,
+                                "convention": "6 dk dv + 64 (3 dk + 2 dv) per token-head"}},
         "gpu_launches": launches_per_step * K,
         "clocks": clk.summary(),
     }

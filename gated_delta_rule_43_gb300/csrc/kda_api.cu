@@ -14,9 +14,16 @@ cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const vo
                               const void *v, const void *z, const void *beta,
                               const float *A_log, const int32_t *cu, int N, int64_t T_tot, int H,
                               const float *h0, float *hT, void *o, StatusWord *st,
-                              cudaStream_t s);
+                              cudaStream_t s, EventRec *rec);
 cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
                         StatusWord *st, cudaStream_t s);
+size_t tc_record_bytes();
+cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
+                            const void *beta, const float *A_log, const int32_t *cu,
+                            const int32_t *chunk_off, int N, int64_t slots, int H,
+                            const float *h0, float *S_run, void *o, uint8_t *records,
+                            int64_t window, StatusWord *st, cudaStream_t s, EventRec *rec);
+int64_t chunk_slots(int64_t T_tot, int N, int C);
 cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
                         const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
                         float *G, StatusWord *st, cudaStream_t s);
@@ -32,16 +39,42 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline bool head_ok(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
+// Chunk length of the tensor-core path and the byte budget of one window of
+// chunk records: a window is produced by the prep kernel and consumed by the
+// chain kernel right after, so it is sized to stay resident in the 129 MB L2.
+constexpr int kTcChunk = 64;
+constexpr size_t kTcWindowBudget = 80u << 20;
+
+bool use_tc(int32_t dtype, int32_t dk, int32_t dv) {
+    return dtype == KDA_BF16 && dk == 128 && dv == 128;
+}
+
 struct ChunkLayout {
-    size_t plan_off, plan_bytes, total;
+    size_t plan_off, plan_bytes;
+    size_t state_off, state_bytes;   // running state of the tensor-core path
+    size_t rec_off, rec_bytes;       // one window of chunk records
+    int64_t slots, window;
+    size_t total;
 };
 
-ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv) {
-    (void)T; (void)H; (void)dk; (void)dv;
-    ChunkLayout L;
+ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv,
+                         int32_t dtype) {
+    ChunkLayout L{};
     L.plan_off = kHeaderBytes;
-    L.plan_bytes = round_up(sizeof(int32_t) * ((size_t)N + 1), 256);
-    L.total = L.plan_off + L.plan_bytes;
+    L.plan_bytes = round_up(sizeof(int32_t) * ((size_t)N + 1), 1024);
+    L.state_off = L.plan_off + L.plan_bytes;
+    L.rec_off = L.state_off;
+    if (use_tc(dtype, dk, dv)) {
+        L.state_bytes = round_up((size_t)N * H * dk * dv * sizeof(float), 1024);
+        L.rec_off = L.state_off + L.state_bytes;
+        L.slots = chunk_slots(T, N, kTcChunk);
+        const size_t rec = tc_record_bytes() * (size_t)H;
+        int64_t w = (int64_t)(kTcWindowBudget / rec);
+        if (w < 1) w = 1;
+        L.window = L.slots < w ? L.slots : w;
+        L.rec_bytes = (size_t)L.window * rec;
+    }
+    L.total = L.rec_off + L.rec_bytes;
     return L;
 }
 
@@ -50,6 +83,54 @@ kda_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_E
 // Grids over chunk slots use gridDim.x, which is limited to 2^31 - 1.
 bool chunk_slots_overflow(int64_t T, int32_t N, int32_t C) {
     return (T + C - 1) / C + N > 0x7fffffffLL;
+}
+
+// The chunked forward behind kda_chunk_fwd and kda_chunk_fwd_profiled; `rec`
+// (optional) records timing events around every kernel it launches.
+kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const void *z,
+                          const void *beta, const float *A_log, const int32_t *cu_seqlens,
+                          int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
+                          int32_t dv, int32_t dtype, const float *initial_state,
+                          float *final_state, void *o, void *workspace, size_t workspace_bytes,
+                          void *stream, EventRec *rec) {
+    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
+    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && num_seqs == 0) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > ((int64_t)1 << 40) / ((int64_t)H * (dk > dv ? dk : dv)))
+        return KDA_ERR_INVALID_ARG;
+    if (!A_log || !cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
+    if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
+    const void *al16[] = {q, k, v, z, o, initial_state, final_state};
+    for (const void *p : al16)
+        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
+    if (!aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
+    if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
+    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype);
+    if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
+    if (chunk_slots_overflow(total_tokens, num_seqs, kTcChunk)) return KDA_ERR_INVALID_ARG;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    StatusWord *st = (StatusWord *)workspace;
+    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
+    if (use_tc(dtype, dk, dv)) {
+        uint8_t *ws = (uint8_t *)workspace;
+        int32_t *chunk_off = (int32_t *)(ws + L.plan_off);
+        float *S_run = final_state ? final_state : (float *)(ws + L.state_off);
+        if (rec) rec->mark();
+        e = launch_plan(cu_seqlens, num_seqs, total_tokens, kTcChunk, chunk_off, st, s);
+        if (e != cudaSuccess) return KDA_ERR_CUDA;
+        if (rec) rec->mark();
+        e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs, L.slots, H,
+                            initial_state, S_run, o, ws + L.rec_off, L.window, st, s, rec);
+        return cuda_status(e);
+    }
+    if (rec) rec->mark();
+    e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
+                          total_tokens, H, initial_state, final_state, o, st, s, rec);
+    return cuda_status(e);
 }
 
 }  // namespace
@@ -77,7 +158,7 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
     if (total_tokens < 0 || num_seqs < 0 || H <= 0 || !head_ok(dk) || !head_ok(dv) ||
         (dtype != KDA_F32 && dtype != KDA_BF16))
         return 0;
-    return chunk_layout(total_tokens, num_seqs, H, dk, dv).total;
+    return chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype).total;
 }
 
 size_t kda_decode_workspace_size(void) { return kHeaderBytes; }
@@ -88,30 +169,28 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                          int32_t dv, int32_t dtype, const float *initial_state,
                          float *final_state, void *o, void *workspace, size_t workspace_bytes,
                          void *stream) {
-    if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
-    if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
-    if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > 0 && num_seqs == 0) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > ((int64_t)1 << 40) / ((int64_t)H * (dk > dv ? dk : dv)))
-        return KDA_ERR_INVALID_ARG;
-    if (!A_log || !cu_seqlens || !workspace) return KDA_ERR_INVALID_ARG;
-    if (total_tokens > 0 && (!q || !k || !v || !z || !beta || !o)) return KDA_ERR_INVALID_ARG;
-    const void *al16[] = {q, k, v, z, o, initial_state, final_state};
-    for (const void *p : al16)
-        if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
-    if (!aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
-    if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
-    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dv);
-    if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
+    return chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
+                          dtype, initial_state, final_state, o, workspace, workspace_bytes, stream,
+                          nullptr);
+}
 
-    cudaStream_t s = (cudaStream_t)stream;
-    StatusWord *st = (StatusWord *)workspace;
-    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
-    if (num_seqs == 0) return KDA_OK;
-    e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
-                          total_tokens, H, initial_state, final_state, o, st, s);
-    return cuda_status(e);
+kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, const void *z,
+                                  const void *beta, const float *A_log,
+                                  const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int64_t total_tokens, int32_t H, int32_t dk, int32_t dv,
+                                  int32_t dtype, const float *initial_state, float *final_state,
+                                  void *o, void *workspace, size_t workspace_bytes, void *stream,
+                                  void *const *events, int32_t n_events, int32_t *n_recorded) {
+    if (!events || n_events < 1 || !n_recorded) return KDA_ERR_INVALID_ARG;
+    EventRec rec;
+    rec.ev = (cudaEvent_t *)events;
+    rec.cap = n_events;
+    rec.s = (cudaStream_t)stream;
+    const kda_status r = chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
+                                        total_tokens, H, dk, dv, dtype, initial_state,
+                                        final_state, o, workspace, workspace_bytes, stream, &rec);
+    *n_recorded = rec.used;
+    return r;
 }
 
 kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
@@ -152,7 +231,7 @@ kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_
     if (!aligned(z, 16) || !aligned(g_cumsum, 16) || !aligned(workspace, 256))
         return KDA_ERR_INVALID_ARG;
     if ((const void *)g_cumsum == z && g_cumsum) return KDA_ERR_INVALID_ARG;
-    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dk);
+    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dk, dtype);
     if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
     if (chunk_slots_overflow(total_tokens, num_seqs, chunk)) return KDA_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;

@@ -201,7 +201,7 @@ template <int DK, typename T>
 static cudaError_t launch_simt_t(const void *q, const void *k, const void *v, const void *z,
                                  const void *beta, const float *A_log, const int32_t *cu, int N,
                                  int64_t T_tot, int H, int dv, const float *h0, float *hT,
-                                 void *o, StatusWord *st, cudaStream_t s) {
+                                 void *o, StatusWord *st, cudaStream_t s, EventRec *rec) {
     const size_t smem = simt_smem_floats<DK>() * sizeof(float);
     auto kern = chunk_fwd_simt_kernel<DK, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -212,6 +212,7 @@ static cudaError_t launch_simt_t(const void *q, const void *k, const void *v, co
     kern<<<(unsigned)grid, kSimtThreads, smem, s>>>((const T *)q, (const T *)k, (const T *)v,
                                                     (const T *)z, (const T *)beta, A_log, cu, N,
                                                     T_tot, H, dv, h0, hT, (T *)o, st);
+    if (rec) rec->mark();
     return cudaGetLastError();
 }
 
@@ -219,14 +220,14 @@ cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const vo
                               const void *v, const void *z, const void *beta,
                               const float *A_log, const int32_t *cu, int N, int64_t T_tot, int H,
                               const float *h0, float *hT, void *o, StatusWord *st,
-                              cudaStream_t s) {
+                              cudaStream_t s, EventRec *rec) {
 #define KDA_SIMT(DK_)                                                                          \
     if (dk == DK_) {                                                                           \
         if (dtype == KDA_BF16)                                                                 \
             return launch_simt_t<DK_, __nv_bfloat16>(q, k, v, z, beta, A_log, cu, N, T_tot, H, \
-                                                     dv, h0, hT, o, st, s);                    \
+                                                     dv, h0, hT, o, st, s, rec);               \
         return launch_simt_t<DK_, float>(q, k, v, z, beta, A_log, cu, N, T_tot, H, dv, h0, hT, \
-                                         o, st, s);                                            \
+                                         o, st, s, rec);                                       \
     }
     KDA_SIMT(32) KDA_SIMT(64) KDA_SIMT(128)
 #undef KDA_SIMT

@@ -25,6 +25,18 @@ constexpr float kGMin = -5.0f;
 constexpr float kTileDecayBound = -80.0f;
 constexpr int kTile = 16;
 
+// Optional timing hook: records caller-created CUDA events on the launch stream
+// before the first kernel and after every kernel of one call.
+struct EventRec {
+    cudaEvent_t *ev = nullptr;
+    int cap = 0;
+    int used = 0;
+    cudaStream_t s = nullptr;
+    void mark() {
+        if (ev && used < cap) cudaEventRecord(ev[used++], s);
+    }
+};
+
 __device__ __forceinline__ void report(StatusWord *st, uint32_t code, long long info,
                                        uint32_t site = 0) {
     if (st == nullptr) return;

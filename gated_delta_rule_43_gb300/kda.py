@@ -29,6 +29,9 @@ SIGNATURES = {
     "kda_chunk_fwd_workspace_size": (SZ, [I64, I32, I32, I32, I32, I32]),
     "kda_chunk_fwd": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P, P, SZ,
                             P]),
+    "kda_chunk_fwd_profiled": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P,
+                                     P, P, SZ, P, ctypes.POINTER(ctypes.c_void_p), I32,
+                                     ctypes.POINTER(ctypes.c_int32)]),
     "kda_decode_workspace_size": (SZ, []),
     "kda_decode_step": (I32, [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P]),
     "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, P, P, SZ, P]),
@@ -137,6 +140,30 @@ def chunk_fwd(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None, *,
     if check:
         query_status(workspace, stream, raise_on_error=True)
     return o, final_state
+
+
+def chunk_fwd_profiled(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state,
+                       workspace, events, stream=None) -> int:
+    """kda_chunk_fwd with CUDA events recorded around each kernel it launches.
+
+    `events` is a list of torch.cuda.Event(enable_timing=True); returns how many
+    were recorded (events[0] before the first kernel, events[i] after the i-th).
+    """
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    used = ctypes.c_int32(0)
+    rc = lib.kda_chunk_fwd_profiled(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),
+                                    _ptr(cu_seqlens), N, T, H, dk, dv, _DT[q.dtype],
+                                    _ptr(initial_state), _ptr(final_state), _ptr(o),
+                                    _ptr(workspace), workspace.numel(), _stream(stream),
+                                    handles, len(events), ctypes.byref(used))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_profiled")
+    return used.value
 
 
 def decode_step(q, k, v, z, beta, A_log, state, *, o=None, workspace=None, stream=None):

@@ -106,6 +106,26 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                          float *final_state, void *o, void *workspace, size_t workspace_bytes,
                          void *stream);
 
+/*
+ * kda_chunk_fwd with per-kernel timing: identical arguments and results, plus
+ * `events`, an array of n_events caller-created cudaEvent_t handles (created
+ * with timing enabled).  The call records events[0] on `stream` before its
+ * first kernel and events[i] after its i-th kernel, for as many kernels as fit,
+ * and writes the number of events recorded to *n_recorded (host pointer).  The
+ * kernels of one call on the tensor-core path are, in order: the chunk plan,
+ * the running-state initialisation (absent when initial_state aliases
+ * final_state), then one (prep, chain) pair per window of chunk records; on
+ * the CUDA-core path, one chunked kernel.  Used by the benchmark to time the
+ * dominant kernel on its own launch stream.
+ */
+kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, const void *z,
+                                  const void *beta, const float *A_log,
+                                  const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int64_t total_tokens, int32_t H, int32_t dk, int32_t dv,
+                                  int32_t dtype, const float *initial_state, float *final_state,
+                                  void *o, void *workspace, size_t workspace_bytes, void *stream,
+                                  void *const *events, int32_t n_events, int32_t *n_recorded);
+
 /* Bytes of workspace kda_decode_step needs (the status word only). */
 size_t kda_decode_workspace_size(void);
 

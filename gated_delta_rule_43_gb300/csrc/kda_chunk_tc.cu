@@ -59,23 +59,26 @@ constexpr int PREP_THREADS = 256;
 // shared-memory map of the prep kernel (offsets from a 1024-aligned base)
 constexpr uint32_t P_KRQR = 0;          // K-major [128][128] row-scaled K/Q, tile a -> rows 32a..32a+31
 constexpr uint32_t P_KC = 32768;        // column-scaled K images, a = 0..3: [16(a+1)][128]
+constexpr uint32_t P_RAW = 32768;       // (before them) raw bf16 tiles q, k, z: 3 x [64][128]
 constexpr uint32_t P_AS = 0;            // (after the A/P products) fp32 A [64][65]
 constexpr uint32_t P_TS = 16640;        //   fp32 T [64][65]
 constexpr uint32_t P_XS = 33280;        //   fp32 scratch [4][16][17]
 constexpr uint32_t P_UST = 37888;       //   fp32 Ut staging [4][64][32]
-constexpr uint32_t P_KF = 73728;        // fp32 [64][128] k / exp(G - ref)
-constexpr uint32_t P_KGV = 106496;      // MN-major [64][256]: K*Gam (n < 128) | V (n >= 128)
-constexpr uint32_t P_WQ = 139264;       // K-major [128][128]
-constexpr uint32_t P_KT = 172032;       // MN-major [64][128]
-constexpr uint32_t P_TB = 188416;       // K-major [64][64] T diag(b); rows 64..127 of the M=128
-constexpr uint32_t P_P = 196608;        //   operand read the P image that follows (ignored rows)
-constexpr uint32_t P_REF = 204800;      // fp32 [5][128]: ref_0..ref_3, G_C
-constexpr uint32_t P_RT = 207360;       // fp32 [10][128]: exp(ref_a - ref_b) (b<a), exp(G_C - ref_b)
-constexpr uint32_t P_BETA = 212480;     // fp32 [64]
-constexpr uint32_t P_BAR = 212736;      // 2 mbarriers + TMEM slot
-constexpr uint32_t P_SMEM = 212800 + 1024;
+constexpr uint32_t P_KF = 81920;        // fp32 [64][128] k / exp(G - ref)
+constexpr uint32_t P_KGV = 114688;      // MN-major [64][256]: K*Gam (n < 128) | V (n >= 128)
+constexpr uint32_t P_WQ = 147456;       // K-major [128][128]
+constexpr uint32_t P_KT = 180224;       // MN-major [64][128]
+constexpr uint32_t P_TB = 196608;       // K-major [64][64] T diag(b); rows 64..127 of the M=128
+constexpr uint32_t P_P = 204800;        //   operand read the P image that follows (ignored rows)
+constexpr uint32_t P_REF = 212992;      // fp32 [5][128]: ref_0..ref_3, G_C
+constexpr uint32_t P_RT = 215552;       // fp32 [10][128]: exp(ref_a - ref_b) (b<a), exp(G_C - ref_b)
+constexpr uint32_t P_BETA = 220672;     // fp32 [64]
+constexpr uint32_t P_HALF = 220928;     // fp32 [128] g-sum of rows 0..31 per channel
+constexpr uint32_t P_BAR = 221440;      // 2 mbarriers + TMEM slot
+constexpr uint32_t P_SMEM = 221504 + 1024;
 static_assert(P_UST + 4 * 64 * 32 * 4 <= P_KF, "prep smem reuse overlaps");
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_KF, "column-scaled K images overflow");
+static_assert(P_RAW + 3 * 16384 <= P_KF, "raw tiles overflow");
 static_assert(P_XS >= P_TS + 64 * 65 * 4 && P_UST >= P_XS + 4 * 16 * 17 * 4, "solve scratch");
 static_assert(P_P == P_TB + 8192, "rows 64..127 of the T diag(b) operand must be valid smem");
 static_assert(P_SMEM <= 232448, "prep kernel exceeds 227 KB of shared memory");
@@ -133,28 +136,60 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tc_fence_before();
     }
 
-    // ---- (1) gate, tile references and decay-scaled operands
-    if (tid < DK) {
-        const int c = tid;
+    // ---- (0) stage the chunk's q, k, z tiles (row-major bf16) and V (into the MN-major
+    //          [K*Gam | V] image) with 16-byte loads; rows past the sequence end are zero
+    {
+        uint8_t *raw = sm + P_RAW;
+        for (int e = tid; e < 4 * C * 16; e += PREP_THREADS) {
+            const int tsel = e / (C * 16), rem = e % (C * 16);
+            const int r = rem / 16, c8 = (rem % 16) * 8;
+            const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
+            uint4 val = make_uint4(0, 0, 0, 0);
+            if (r < L) val = *reinterpret_cast<const uint4 *>(src + ((t0 + r) * H + h) * (int64_t)DK + c8);
+            if (tsel < 3)
+                *reinterpret_cast<uint4 *>(raw + tsel * 16384 + r * 256 + c8 * 2) = val;
+            else
+                *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c8, 64)) = val;
+        }
+        if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+    }
+    __syncthreads();
+
+    // ---- (1) gate, tile references and decay-scaled operands: thread (c, half) walks
+    //          rows 32*half .. 32*half+31 of channel c
+    {
+        const int c = tid & (DK - 1), half = tid >> 7;
+        const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(sm + P_RAW);
+        const __nv_bfloat16 *rk = rq + C * DK;
+        const __nv_bfloat16 *rz = rk + C * DK;
+        float *HALF = reinterpret_cast<float *>(sm + P_HALF);
         const float expA = expf(A_log[h]);
-        float run = 0.f, ref = 0.f, trun = 0.f;  // chunk cumsum, tile reference, in-tile cumsum
-        for (int r = 0; r < C; ++r) {
-            float kk = 0.f, qq = 0.f, g = 0.f;
-            if (r < L) {
-                const int64_t idx = ((t0 + r) * H + h) * (int64_t)DK + c;
-                kk = __bfloat162float(k[idx]);
-                qq = __bfloat162float(q[idx]);
-                g = gate(__bfloat162float(z[idx]), expA);
-            }
+        float g[32];
+        float part = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * half + i;
+            g[i] = r < L ? gate(__bfloat162float(rz[r * DK + c]), expA) : 0.f;
+            part += g[i];
+        }
+        if (half == 0) HALF[c] = part;
+        __syncthreads();
+        float run = half ? HALF[c] : 0.f;   // chunk cumsum before this thread's first row
+        float ref = run, trun = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const int r = 32 * half + i;
             const int a = r >> 4;
-            if ((r & 15) == 0) {
+            if ((i & 15) == 0) {
                 ref = run;
                 trun = 0.f;
                 REF[a * DK + c] = ref;
             }
-            run += g;
-            trun += g;
+            run += g[i];
+            trun += g[i];
             if (r < L && !decay_ok(trun)) report(st, KDA_ERR_DECAY_RANGE, (t0 + r) * H + h, 5);
+            const float kk = __bfloat162float(rk[r * DK + c]);
+            const float qq = __bfloat162float(rq[r * DK + c]);
             const float F = expf(trun);          // exp(G_r - ref_a) in [e^-80, 1]
             const float Gm = expf(run);          // exp(G_r) <= 1 (may underflow)
             const uint32_t row = 32 * a + (r & 15);
@@ -164,18 +199,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             st_bf16(sm + P_WQ, sw128_offset(64 + r, c, 128), qq * Gm);
             st_bf16(sm + P_KGV, sw128_offset(r, c, 64), kk * Gm);
         }
-        REF[4 * DK + c] = run;
-        *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
-    } else {
-        // V tile into the n = 128..255 half of the MN-major [K*Gam | V] image
-        const int t = tid - DK;
-        for (int e = t; e < C * (DV / 8); e += PREP_THREADS - DK) {
-            const int r = e / (DV / 8), j8 = (e % (DV / 8)) * 8;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < L) val = *reinterpret_cast<const uint4 *>(v + ((t0 + r) * H + h) * (int64_t)DV + j8);
-            *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + j8, 64)) = val;
+        if (half == 1) {
+            REF[4 * DK + c] = run;
+            *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
         }
-        if (t < C) BETA[t] = t < L ? __bfloat162float(beta[(t0 + t) * H + h]) : 0.f;
     }
     __syncthreads();
     tc_fence_after();

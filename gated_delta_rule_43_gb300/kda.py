@@ -32,6 +32,8 @@ SIGNATURES = {
     "kda_chunk_fwd_profiled": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P,
                                      P, P, SZ, P, ctypes.POINTER(ctypes.c_void_p), I32,
                                      ctypes.POINTER(ctypes.c_int32)]),
+    "kda_chunk_fwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P,
+                                    P, P]),
     "kda_decode_workspace_size": (SZ, []),
     "kda_decode_step": (I32, [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P]),
     "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, P, P, SZ, P]),
@@ -164,6 +166,28 @@ def chunk_fwd_profiled(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, fi
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd_profiled")
     return used.value
+
+
+def chunk_fwd_noalloc(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state,
+                      status_out=None, stream=None):
+    """kda_chunk_fwd_noalloc: the chunked forward with the library's own fixed scratch.
+
+    For callers that cannot allocate device memory; o, final_state and the
+    optional 16-byte status_out buffer are supplied by the caller.  Work on the
+    shared scratch must not overlap between calls (serialise them).
+    """
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, status_out)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),
+                                   _ptr(cu_seqlens), N, T, H, dk, dv, _DT[q.dtype],
+                                   _ptr(initial_state), _ptr(final_state), _ptr(o),
+                                   _ptr(status_out), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_noalloc")
+    return o, final_state
 
 
 def decode_step(q, k, v, z, beta, A_log, state, *, o=None, workspace=None, stream=None):

@@ -126,6 +126,53 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
                                   void *o, void *workspace, size_t workspace_bytes, void *stream,
                                   void *const *events, int32_t n_events, int32_t *n_recorded);
 
+/*
+ * Size of the scratch array behind kda_chunk_fwd_noalloc: 32 MiB, held on
+ * every GPU that loads this library until the process exits.
+ */
+#define KDA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * kda_chunk_fwd for callers that cannot allocate device memory.  (The pages
+ * have no counterpart: this is an interface convenience, not part of the
+ * method.)
+ *
+ * Who needs it: code that is handed its input and output buffers and nothing
+ * else -- a plug-in inside a host application that owns every device
+ * allocation, or a serving loop that must not call cudaMalloc after start-up
+ * (cudaMalloc synchronises the device and can fail under memory pressure).
+ * Such callers cannot supply kda_chunk_fwd's workspace.  This entry runs the
+ * same kernels with the same results, and takes its scratch (status word,
+ * chunk plan, running state, chunk records) from a fixed array of
+ * KDA_NOALLOC_SCRATCH_BYTES owned by the library.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ * Arguments are those of kda_chunk_fwd without the workspace, plus:
+ *   status_out  NULL, or a device buffer of >= 16 bytes (16-byte aligned)
+ *               that receives the call's status word when the call's work
+ *               completes; read it with kda_query_status(status_out, ...).
+ * Limits: the problem must fit the array.  On the tensor-core path (bf16,
+ * dk = dv = 128) the chunk plan ((num_seqs + 1) int32), the running state
+ * (num_seqs * H * 64 KiB, only when final_state is NULL) and at least one
+ * chunk record per head (H * 90,624 bytes) must fit in 32 MiB; larger
+ * problems are rejected with KDA_ERR_INVALID_ARG before anything is launched.
+ * Fewer records fit than in a caller-sized workspace, so long inputs run in
+ * more, smaller windows.
+ * Set-up: the first call on each device looks up the array's device address
+ * (with that device current) and caches it; make that first call before any
+ * stream capture.
+ * Concurrency: every call uses the same array, which keeps the previous
+ * call's contents (each call clears what it needs).  Calls whose work can
+ * overlap on the GPU -- on different streams, or from threads that do not
+ * order their launches -- race on the array and must be serialised.
+ */
+kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, const void *z,
+                                 const void *beta, const float *A_log,
+                                 const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t H, int32_t dk, int32_t dv,
+                                 int32_t dtype, const float *initial_state, float *final_state,
+                                 void *o, void *status_out, void *stream);
+
 /* Bytes of workspace kda_decode_step needs (the status word only). */
 size_t kda_decode_workspace_size(void);
 

@@ -156,6 +156,9 @@ def chunk_fwd_profiled(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, fi
     T, H, dk = q.shape
     dv = v.shape[-1]
     N = cu_seqlens.numel() - 1
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record(stream if stream is not None else torch.cuda.current_stream())
     handles = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     used = ctypes.c_int32(0)
     rc = lib.kda_chunk_fwd_profiled(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),

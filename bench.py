@@ -210,6 +210,10 @@ def run_ours(args, rank, world, local):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(K)]
+    for row in kev:                 # torch creates each CUDA event on its first record:
+        for e_ in row:              # do that here, outside the timed region
+            e_.record(stream)
+    torch.cuda.synchronize(dev)
     used = []
     barrier(world)
     torch.cuda.synchronize(dev)

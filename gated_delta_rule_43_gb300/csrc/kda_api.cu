@@ -9,7 +9,8 @@
 namespace kda {
 cudaError_t launch_decode(int dtype, int dk, int dv, const void *q, const void *k,
                           const void *v, const void *z, const void *beta, const float *A_log,
-                          float *state, void *o, int N, int H, cudaStream_t s);
+                          float *state, void *o, int N, int H, const int32_t *slot_idx, int P,
+                          StatusWord *st, cudaStream_t s);
 cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const void *k,
                               const void *v, const void *z, const void *beta,
                               const float *A_log, const int32_t *cu, int N, int64_t T_tot, int H,
@@ -193,13 +194,16 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
     return r;
 }
 
-kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
-                           const void *beta, const float *A_log, float *state, void *o,
-                           int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype,
-                           void *workspace, size_t workspace_bytes, void *stream) {
+// Shared body of kda_decode_step (slot_idx NULL: sequence n owns state n) and
+// kda_decode_step_indexed (sequence n owns slot slot_idx[n] of a pool of P).
+static kda_status decode_impl(const void *q, const void *k, const void *v, const void *z,
+                              const void *beta, const float *A_log, float *state,
+                              const int32_t *slot_idx, int32_t P, void *o, int32_t N,
+                              int32_t H, int32_t dk, int32_t dv, int32_t dtype, void *workspace,
+                              size_t workspace_bytes, void *stream) {
     if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
-    if (N < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
+    if (N < 0 || H <= 0 || P < 0) return KDA_ERR_INVALID_ARG;
     if ((int64_t)N * H > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
     if (!workspace || workspace_bytes < kHeaderBytes || !aligned(workspace, 256))
         return KDA_ERR_INVALID_ARG;
@@ -211,10 +215,30 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
     if (o && (o == q || o == k || o == v || o == z || o == beta || o == (void *)state))
         return KDA_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
-    cudaError_t e = cudaMemsetAsync(workspace, 0, sizeof(StatusWord), s);
+    StatusWord *st = (StatusWord *)workspace;
+    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     if (N == 0) return KDA_OK;
-    return cuda_status(launch_decode(dtype, dk, dv, q, k, v, z, beta, A_log, state, o, N, H, s));
+    return cuda_status(launch_decode(dtype, dk, dv, q, k, v, z, beta, A_log, state, o, N, H,
+                                     slot_idx, P, st, s));
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v, const void *z,
+                           const void *beta, const float *A_log, float *state, void *o,
+                           int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                           void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(q, k, v, z, beta, A_log, state, nullptr, N, o, N, H, dk, dv, dtype,
+                       workspace, workspace_bytes, stream);
+}
+
+kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, const void *z,
+                                   const void *beta, const float *A_log, float *state_pool,
+                                   const int32_t *state_idx, int32_t P, void *o, int32_t N,
+                                   int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    if (N > 0 && !state_idx) return KDA_ERR_INVALID_ARG;
+    return decode_impl(q, k, v, z, beta, A_log, state_pool, state_idx, P, o, N, H, dk, dv,
+                       dtype, workspace, workspace_bytes, stream);
 }
 
 kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_seqlens,

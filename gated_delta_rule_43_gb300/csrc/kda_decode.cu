@@ -9,6 +9,11 @@
 // beta_t) for a single token.  The state is read once and written once: one
 // CTA per (n, h), each thread holding R rows x 4 columns of S in registers
 // between the read and the write, so no column is fetched twice.
+//
+// With a slot index, sequence n reads and writes slot slot_idx[n] of a state
+// pool [P, H, dk, dv] instead of state n (the fixed-size KDA states of the
+// paged hybrid cache, dev.to page "Kimi K3 Architecture...", section
+// "Infrastructure and Training/Inference Mechanics", serving engine).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -20,7 +25,8 @@ __global__ void __launch_bounds__(kDecodeThreads)
 decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    const T *__restrict__ z, const T *__restrict__ beta,
                    const float *__restrict__ A_log, float *__restrict__ state,
-                   T *__restrict__ o, int H) {
+                   T *__restrict__ o, int H, const int32_t *__restrict__ slot_idx, int P,
+                   StatusWord *st) {
     constexpr int TPR = DV / 4;                 // threads covering one row (float4 each)
     constexpr int RPP = kDecodeThreads / TPR;   // rows covered per pass
     constexpr int R = DK / RPP;                 // rows per thread
@@ -33,14 +39,20 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
     const int nh = blockIdx.x;
     const int h = nh % H;
+    const int n = nh / H;
     const int tid = threadIdx.x;
     const int64_t kb = (int64_t)nh * DK;
     const int64_t vb = (int64_t)nh * DV;
+    const int slot = slot_idx ? slot_idx[n] : n;
+    if (slot < 0 || slot >= P) {
+        if (tid == 0 && h == 0) report(st, KDA_ERR_INVALID_ARG, n, 20);
+        return;
+    }
 
     // Issue the state loads first: they are the bulk of the traffic.
     const int c4 = tid % TPR;
     const int rg = tid / TPR;
-    float4 *S4 = reinterpret_cast<float4 *>(state + (int64_t)nh * DK * DV);
+    float4 *S4 = reinterpret_cast<float4 *>(state + ((int64_t)slot * H + h) * DK * DV);
     float4 s[R];
 #pragma unroll
     for (int p = 0; p < R; ++p) s[p] = __ldcs(S4 + (int64_t)(rg + p * RPP) * TPR + c4);
@@ -103,20 +115,24 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 template <int DK, int DV, typename T>
 static cudaError_t launch_decode_t(const void *q, const void *k, const void *v, const void *z,
                                    const void *beta, const float *A_log, float *state, void *o,
-                                   int N, int H, cudaStream_t stream) {
+                                   int N, int H, const int32_t *slot_idx, int P, StatusWord *st,
+                                   cudaStream_t stream) {
     decode_step_kernel<DK, DV, T><<<(unsigned)((int64_t)N * H), kDecodeThreads, 0, stream>>>(
         (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)beta, A_log, state,
-        (T *)o, H);
+        (T *)o, H, slot_idx, P, st);
     return cudaGetLastError();
 }
 
 template <typename T>
 static cudaError_t launch_decode_dt(int dk, int dv, const void *q, const void *k, const void *v,
                                     const void *z, const void *beta, const float *A_log,
-                                    float *state, void *o, int N, int H, cudaStream_t s) {
+                                    float *state, void *o, int N, int H,
+                                    const int32_t *slot_idx, int P, StatusWord *st,
+                                    cudaStream_t s) {
 #define KDA_DEC(DK_, DV_)                                                                    \
     if (dk == DK_ && dv == DV_)                                                              \
-        return launch_decode_t<DK_, DV_, T>(q, k, v, z, beta, A_log, state, o, N, H, s);
+        return launch_decode_t<DK_, DV_, T>(q, k, v, z, beta, A_log, state, o, N, H, slot_idx, \
+                                            P, st, s);
     KDA_DEC(32, 32) KDA_DEC(32, 64) KDA_DEC(32, 128)
     KDA_DEC(64, 32) KDA_DEC(64, 64) KDA_DEC(64, 128)
     KDA_DEC(128, 32) KDA_DEC(128, 64) KDA_DEC(128, 128)
@@ -126,11 +142,13 @@ static cudaError_t launch_decode_dt(int dk, int dv, const void *q, const void *k
 
 cudaError_t launch_decode(int dtype, int dk, int dv, const void *q, const void *k,
                           const void *v, const void *z, const void *beta, const float *A_log,
-                          float *state, void *o, int N, int H, cudaStream_t s) {
+                          float *state, void *o, int N, int H, const int32_t *slot_idx, int P,
+                          StatusWord *st, cudaStream_t s) {
     if (dtype == KDA_BF16)
         return launch_decode_dt<__nv_bfloat16>(dk, dv, q, k, v, z, beta, A_log, state, o, N, H,
-                                               s);
-    return launch_decode_dt<float>(dk, dv, q, k, v, z, beta, A_log, state, o, N, H, s);
+                                               slot_idx, P, st, s);
+    return launch_decode_dt<float>(dk, dv, q, k, v, z, beta, A_log, state, o, N, H, slot_idx, P,
+                                   st, s);
 }
 
 }  // namespace kda

@@ -36,6 +36,8 @@ SIGNATURES = {
                                     P, P]),
     "kda_decode_workspace_size": (SZ, []),
     "kda_decode_step": (I32, [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P]),
+    "kda_decode_step_indexed": (I32, [P, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, P,
+                                      SZ, P]),
     "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, P, P, SZ, P]),
     "kda_query_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int64)]),
 }
@@ -214,6 +216,34 @@ def decode_step(q, k, v, z, beta, A_log, state, *, o=None, workspace=None, strea
                              workspace.numel(), _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_decode_step")
+    return o
+
+
+def decode_step_indexed(q, k, v, z, beta, A_log, state_pool, state_idx, *, o=None,
+                        workspace=None, stream=None, check: bool = False):
+    """One decode step where sequence n owns slot state_idx[n] of state_pool (in place).
+
+    q, k, z [N, H, dk], v [N, H, dv], beta [N, H]; state_pool [P, H, dk, dv] fp32;
+    state_idx [N] int32 (distinct values in [0, P)).  Returns o [N, H, dv].
+    """
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, state_pool, state_idx, o, workspace)
+    N, H, dk = q.shape
+    dv = v.shape[-1]
+    if state_pool.dtype != torch.float32 or state_idx.dtype != torch.int32:
+        raise TypeError("state_pool must be fp32 and state_idx int32")
+    if o is None:
+        o = torch.empty(N, H, dv, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(int(lib.kda_decode_workspace_size()), q.device)
+    rc = lib.kda_decode_step_indexed(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta),
+                                     _ptr(A_log), _ptr(state_pool), _ptr(state_idx),
+                                     state_pool.shape[0], _ptr(o), N, H, dk, dv, _DT[q.dtype],
+                                     _ptr(workspace), workspace.numel(), _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_decode_step_indexed")
+    if check:
+        query_status(workspace, stream, raise_on_error=True)
     return o
 
 

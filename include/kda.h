@@ -197,6 +197,25 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v, const vo
                            void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_decode_step against a pool of states: sequence n advances the state in
+ * slot state_idx[n] of state_pool, which is updated in place.  This is the
+ * KDA half of the serving engine's paged hybrid cache, where fixed-size KDA
+ * states live in pooled memory (dev.to page, section "Infrastructure and
+ * Training/Inference Mechanics", "Serving Engine").
+ *
+ *   state_pool [P, H, dk, dv] fp32          state_idx [N] int32, device, values in [0, P)
+ *   other arguments as kda_decode_step (q, k, z, v, beta, o are per sequence n)
+ * The N indices must be distinct (two sequences sharing a slot race).  An
+ * index outside [0, P) is recorded as KDA_ERR_INVALID_ARG in the status word
+ * (info = the sequence) and that sequence is skipped.
+ */
+kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, const void *z,
+                                   const void *beta, const float *A_log, float *state_pool,
+                                   const int32_t *state_idx, int32_t P, void *o, int32_t N,
+                                   int32_t H, int32_t dk, int32_t dv, int32_t dtype,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * The gate on its own: g = -5 Sigmoid(exp(A_h) z) per channel and its
  * inclusive cumulative sum restarted every `chunk` tokens (chunks start at
  * each sequence's first token), written as fp32 [total_tokens, H, dk].

@@ -79,3 +79,58 @@ def test_prefill_then_decode_handoff(dtype):
     tol = TOL[dtype]
     assert rel_l2(to_f64(torch.cat(outs)), to_f64(o_all)) <= tol
     assert rel_l2(to_f64(S), to_f64(s_all)) <= tol
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_indexed_state_pool(dtype):
+    """Sequence n advances slot idx[n] of a state pool; other slots are untouched."""
+    N, H, dk, dv, P = 4, 3, 128, 64, 7
+    ds = inputs.DecodeStream(N, H, dk, dv, dtype, seed=12, device=DEV)
+    g = torch.Generator(device=DEV).manual_seed(13)
+    pool = torch.randn(P, H, dk, dv, device=DEV, generator=g) * 0.1
+    idx = torch.tensor([5, 0, 3, 6], dtype=torch.int32, device=DEV)
+    dense = pool.index_select(0, idx.long()).clone()
+    before = pool.clone()
+    for _ in range(3):
+        x = ds.step()
+        o_pool = kda.decode_step_indexed(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log,
+                                         pool, idx, check=True)
+        o_dense = kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, dense)
+        assert torch.equal(o_pool, o_dense)
+    assert torch.equal(pool.index_select(0, idx.long()), dense)
+    untouched = [s for s in range(P) if s not in idx.tolist()]
+    assert torch.equal(pool[untouched], before[untouched])
+
+
+def test_decode_indexed_rejects_bad_slot():
+    ds = inputs.DecodeStream(2, 1, 32, 32, "f32", seed=14, device=DEV)
+    pool = torch.zeros(3, 1, 32, 32, device=DEV)
+    idx = torch.tensor([1, 3], dtype=torch.int32, device=DEV)   # 3 is outside [0, 3)
+    x = ds.step()
+    with pytest.raises(kda.KdaError) as ei:
+        kda.decode_step_indexed(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, pool, idx,
+                                check=True)
+    assert ei.value.code == kda.KDA_ERR_INVALID_ARG and ei.value.info == 1
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_multi_token_decode_through_chunk_fwd(dtype):
+    """k tokens per sequence against the resident state in one in-place chunked call
+    (initial_state aliasing final_state) equal k single-token decode steps."""
+    N, H, dk, dv, kt = 6, 2, 128, 128, 5
+    d = inputs.make_prefill([kt] * N, H=H, dk=dk, dv=dv, dtype=dtype, seed=15, h0_sigma=0.1,
+                            device=DEV)
+    S_multi = d["h0"].clone()
+    o_multi, _ = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                               d["cu_seqlens"], S_multi, final_state=S_multi, check=True)
+    S_step = d["h0"].clone()
+    outs = []
+    for t in range(kt):
+        rows = torch.arange(N, device=DEV) * kt + t
+        sel = {n_: d[n_].index_select(0, rows) for n_ in ("q", "k", "v", "z", "beta")}
+        outs.append(kda.decode_step(sel["q"], sel["k"], sel["v"], sel["z"], sel["beta"],
+                                    d["A_log"], S_step))
+    o_step = torch.stack(outs, 1).reshape(N * kt, H, dv)
+    tol = TOL[dtype]
+    assert rel_l2(to_f64(o_multi), to_f64(o_step)) <= tol
+    assert rel_l2(to_f64(S_multi), to_f64(S_step)) <= tol

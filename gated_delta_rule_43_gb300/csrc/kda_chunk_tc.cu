@@ -56,35 +56,53 @@ constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
 constexpr int PREP_THREADS = 256;
-// shared-memory map of the prep kernel (offsets from a 1024-aligned base)
-constexpr uint32_t P_KRQR = 0;          // K-major [128][128] row-scaled K/Q, tile a -> rows 32a..32a+31
-constexpr uint32_t P_KC = 32768;        // column-scaled K images, a = 0..3: [16(a+1)][128]
-constexpr uint32_t P_RAW = 32768;       // (before them) raw bf16 tiles q, k, z: 3 x [64][128]
-constexpr uint32_t P_AS = 0;            // (after the A/P products) fp32 A [64][65]
-constexpr uint32_t P_TS = 16640;        //   fp32 T [64][65]
-constexpr uint32_t P_XS = 33280;        //   fp32 scratch [4][16][17]
-constexpr uint32_t P_UST = 37888;       //   fp32 Ut staging [4][64][32]
-constexpr uint32_t P_KF = 81920;        // fp32 [64][128] k / exp(G - ref)
-constexpr uint32_t P_KGV = 114688;      // MN-major [64][256]: K*Gam (n < 128) | V (n >= 128)
-constexpr uint32_t P_WQ = 147456;       // K-major [128][128]
-constexpr uint32_t P_KT = 180224;       // MN-major [64][128]
-constexpr uint32_t P_TB = 196608;       // K-major [64][64] T diag(b); rows 64..127 of the M=128
-constexpr uint32_t P_P = 204800;        //   operand read the P image that follows (ignored rows)
-constexpr uint32_t P_REF = 212992;      // fp32 [5][128]: ref_0..ref_3, G_C
-constexpr uint32_t P_RT = 215552;       // fp32 [10][128]: exp(ref_a - ref_b) (b<a), exp(G_C - ref_b)
-constexpr uint32_t P_BETA = 220672;     // fp32 [64]
-constexpr uint32_t P_HALF = 220928;     // fp32 [128] g-sum of rows 0..31 per channel
-constexpr uint32_t P_BAR = 221440;      // 2 mbarriers + TMEM slot
-constexpr uint32_t P_SMEM = 221504 + 1024;
-static_assert(P_UST + 4 * 64 * 32 * 4 <= P_KF, "prep smem reuse overlaps");
-static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_KF, "column-scaled K images overflow");
-static_assert(P_RAW + 3 * 16384 <= P_KF, "raw tiles overflow");
-static_assert(P_XS >= P_TS + 64 * 65 * 4 && P_UST >= P_XS + 4 * 16 * 17 * 4, "solve scratch");
-static_assert(P_P == P_TB + 8192, "rows 64..127 of the T diag(b) operand must be valid smem");
-static_assert(P_SMEM <= 232448, "prep kernel exceeds 227 KB of shared memory");
+// Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
+// CTAs fit on one SM.  Regions are reused once the A/P products have completed.
+constexpr uint32_t P_BAR = 0;           // 2 mbarriers, TMEM slot
+constexpr uint32_t P_TOT = 1024;        // fp32 [4][128]  per-tile sums of g
+constexpr uint32_t P_REF = 3072;        // fp32 [5][128]  ref_0..ref_3 (cumsum before tile a), G_C
+constexpr uint32_t P_ER = 5632;         // fp32 [4][128]  exp(ref_a)
+constexpr uint32_t P_RT = 7680;         // fp32 [6][128]  exp(ref_a' - ref_a), a < a'
+constexpr uint32_t P_KTF = 10752;       // fp32 [4][128]  exp(G_C - ref_a)
+constexpr uint32_t P_BETA = 12800;      // fp32 [64]
+constexpr uint32_t P_KRQR = 13312;      // K-major [128][128] row-scaled K/Q: tile a -> rows 32a..32a+31
+constexpr uint32_t P_KC = 46080;        // column-scaled K images, a = 0..3: [16(a+1)][128]
+constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64][256]: K*Gam | V
+constexpr uint32_t P_AS = 46080;        //   fp32 A [64][65]
+constexpr uint32_t P_TS = 62720;        //   fp32 T [64][65]
+constexpr uint32_t P_XS = 79360;        //   fp32 [3][16][17] level scratch
+constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
+constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
+constexpr uint32_t P_SMEM = P_END + 1024;
+static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
+static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * 65 * 4 <= P_TS, "prep smem reuse overlaps");
+static_assert(P_TS + 64 * 65 * 4 <= P_XS && P_XS + 3 * 16 * 17 * 4 <= P_TB, "solve scratch");
+static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
+static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
+}
+__device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
+    uint4 r;
+    __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+    return r;
+}
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&x)[8]) {
+    const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(p[i]);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+__device__ __forceinline__ void ld8(const float *src, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(src)[0];
+    const float4 b = reinterpret_cast<const float4 *>(src)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
 // chunk slot -> (sequence, first token, valid rows); false when the slot is unused
@@ -102,7 +120,12 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
     return L > 0;
 }
 
-__global__ void __launch_bounds__(PREP_THREADS, 1)
+// One CTA per (chunk slot, head).  Work split for the element-wise passes:
+// warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2; lane l
+// takes row 16a + (l & 15); its four units are 8-channel chunks
+// ch = 8 (w >> 2) + 2u + (l >> 4), u = 0..3.  Scans over the 16 rows of a tile
+// run across the 16 lanes of a half-warp.
+__global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
@@ -118,9 +141,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (!slot_chunk(cu, chunk_off, N, slot, n, t0, L)) return;
     uint8_t *rec = records + ((size_t)blockIdx.x * H + h) * REC_BYTES;
 
-    float *KF = reinterpret_cast<float *>(sm + P_KF);
+    float *TOT = reinterpret_cast<float *>(sm + P_TOT);
     float *REF = reinterpret_cast<float *>(sm + P_REF);
+    float *ER = reinterpret_cast<float *>(sm + P_ER);
     float *RT = reinterpret_cast<float *>(sm + P_RT);
+    float *KTF = reinterpret_cast<float *>(sm + P_KTF);
     float *BETA = reinterpret_cast<float *>(sm + P_BETA);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_BAR + 16);
@@ -136,216 +161,246 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tc_fence_before();
     }
 
-    // ---- (0) stage the chunk's q, k, z tiles (row-major bf16) and V (into the MN-major
-    //          [K*Gam | V] image) with 16-byte loads; rows past the sequence end are zero
-    {
-        uint8_t *raw = sm + P_RAW;
-        for (int e = tid; e < 4 * C * 16; e += PREP_THREADS) {
-            const int tsel = e / (C * 16), rem = e % (C * 16);
-            const int r = rem / 16, c8 = (rem % 16) * 8;
-            const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (r < L) val = *reinterpret_cast<const uint4 *>(src + ((t0 + r) * H + h) * (int64_t)DK + c8);
-            if (tsel < 3)
-                *reinterpret_cast<uint4 *>(raw + tsel * 16384 + r * 256 + c8 * 2) = val;
-            else
-                *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c8, 64)) = val;
+    const int a = warp & 3;                    // this thread's 16-token tile
+    const int rl = lane & 15;
+    const int r = 16 * a + rl;                 // this thread's row of the chunk
+    const bool valid = r < L;
+    const int64_t row_off = ((t0 + r) * H + h) * (int64_t)DK;
+    const float expA = expf(A_log[h]);
+    if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+
+    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check
+    float trun[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+        float zz[8];
+        unpack8(valid ? *reinterpret_cast<const uint4 *>(z + row_off + 8 * ch) : make_uint4(0, 0, 0, 0), zz);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float x = valid ? gate(zz[i], expA) : 0.f;
+#pragma unroll
+            for (int off = 1; off < 16; off <<= 1) {
+                const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
+                if (rl >= off) x += y;
+            }
+            trun[u][i] = x;
+            if (valid && !decay_ok(x)) report(st, KDA_ERR_DECAY_RANGE, (t0 + r) * H + h, 5);
         }
-        if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+        if (rl == 15) {
+            float4 *dst = reinterpret_cast<float4 *>(TOT + a * DK + 8 * ch);
+            dst[0] = make_float4(trun[u][0], trun[u][1], trun[u][2], trun[u][3]);
+            dst[1] = make_float4(trun[u][4], trun[u][5], trun[u][6], trun[u][7]);
+        }
+    }
+    __syncthreads();
+    // tile references, Gam_C and the per-(tile, channel) factor tables
+    if (tid < DK) {
+        const int c = tid;
+        float run = 0.f, ref[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            ref[t] = run;
+            REF[t * DK + c] = run;
+            ER[t * DK + c] = expf(run);
+            run += TOT[t * DK + c];
+        }
+        REF[4 * DK + c] = run;
+        *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) KTF[t * DK + c] = expf(run - ref[t]);
+        int p = 0;
+#pragma unroll
+        for (int a2 = 1; a2 < 4; ++a2)
+#pragma unroll
+            for (int b = 0; b < a2; ++b, ++p) RT[p * DK + c] = expf(ref[a2] - ref[b]);
     }
     __syncthreads();
 
-    // ---- (1) gate, tile references and decay-scaled operands: thread (c, half) walks
-    //          rows 32*half .. 32*half+31 of channel c
-    {
-        const int c = tid & (DK - 1), half = tid >> 7;
-        const __nv_bfloat16 *rq = reinterpret_cast<const __nv_bfloat16 *>(sm + P_RAW);
-        const __nv_bfloat16 *rk = rq + C * DK;
-        const __nv_bfloat16 *rz = rk + C * DK;
-        float *HALF = reinterpret_cast<float *>(sm + P_HALF);
-        const float expA = expf(A_log[h]);
-        float g[32];
-        float part = 0.f;
+    // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr] (smem), column-scaled K
+    //          images (smem), Q*Gam and K*Gam_C/Gam (straight into the record)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * half + i;
-            g[i] = r < L ? gate(__bfloat162float(rz[r * DK + c]), expA) : 0.f;
-            part += g[i];
-        }
-        if (half == 0) HALF[c] = part;
-        __syncthreads();
-        float run = half ? HALF[c] : 0.f;   // chunk cumsum before this thread's first row
-        float ref = run, trun = 0.f;
+    for (int u = 0; u < 4; ++u) {
+        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+        const int c = 8 * ch;
+        float kk[8], qq[8], er[8], ktf[8];
+        unpack8(valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : make_uint4(0, 0, 0, 0), kk);
+        unpack8(valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : make_uint4(0, 0, 0, 0), qq);
+        ld8(ER + a * DK + c, er);
+        ld8(KTF + a * DK + c, ktf);
+        float kr[8], qr[8], kf[8], qg[8], kt[8];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const int r = 32 * half + i;
-            const int a = r >> 4;
-            if ((i & 15) == 0) {
-                ref = run;
-                trun = 0.f;
-                REF[a * DK + c] = ref;
-            }
-            run += g[i];
-            trun += g[i];
-            if (r < L && !decay_ok(trun)) report(st, KDA_ERR_DECAY_RANGE, (t0 + r) * H + h, 5);
-            const float kk = __bfloat162float(rk[r * DK + c]);
-            const float qq = __bfloat162float(rq[r * DK + c]);
-            const float F = expf(trun);          // exp(G_r - ref_a) in [e^-80, 1]
-            const float Gm = expf(run);          // exp(G_r) <= 1 (may underflow)
-            const uint32_t row = 32 * a + (r & 15);
-            st_bf16(sm + P_KRQR, sw128_offset(row, c, 128), kk * F);
-            st_bf16(sm + P_KRQR, sw128_offset(row + 16, c, 128), qq * F);
-            KF[r * DK + c] = kk / F;             // k_r exp(ref_a - G_r), <= e^80 |k|
-            st_bf16(sm + P_WQ, sw128_offset(64 + r, c, 128), qq * Gm);
-            st_bf16(sm + P_KGV, sw128_offset(r, c, 64), kk * Gm);
+        for (int i = 0; i < 8; ++i) {
+            const float F = __expf(trun[u][i]);       // exp(G_r - ref_a) in [e^-80, 1]
+            const float iF = __expf(-trun[u][i]);     // exp(ref_a - G_r) in [1, e^80]
+            kr[i] = kk[i] * F;
+            qr[i] = qq[i] * F;
+            kf[i] = kk[i] * iF;                       // k_r exp(ref_a - G_r)
+            qg[i] = qq[i] * (er[i] * F);              // q_r exp(G_r)
+            kt[i] = kf[i] * ktf[i];                   // k_r exp(G_C - G_r)
         }
-        if (half == 1) {
-            REF[4 * DK + c] = run;
-            *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
-        }
-    }
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tslot;
-
-    // ---- (2) factor tables: exp(ref_a - ref_b) for b < a (6 pairs), exp(G_C - ref_b)
-    for (int e = tid; e < 10 * DK; e += PREP_THREADS) {
-        const int p = e / DK, c = e % DK;
-        float x;
-        if (p < 6) {
-            const int a = (p < 1) ? 1 : (p < 3) ? 2 : 3;
-            const int b = p - (a * (a - 1)) / 2;
-            x = expf(REF[a * DK + c] - REF[b * DK + c]);
-        } else {
-            x = expf(REF[4 * DK + c] - REF[(p - 6) * DK + c]);
-        }
-        RT[p * DK + c] = x;
-    }
-    __syncthreads();
-    // column-scaled K images: Kc_a[j] = k_j exp(ref_a - G_j), j < 16(a+1)
-    {
-        uint32_t img = P_KC;
-        for (int a = 0; a < 4; ++a) {
-            const int rows = 16 * (a + 1);
-            for (int e = tid; e < rows * DK; e += PREP_THREADS) {
-                const int j = e / DK, c = e % DK, b = j >> 4;
-                float x = KF[j * DK + c];
-                if (b < a) x *= RT[((a * (a - 1)) / 2 + b) * DK + c];
-                st_bf16(sm + img, sw128_offset(j, c, rows), x);
-            }
-            img += rows * 256;
+        const uint32_t row = 32 * a + rl;
+        *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row, c, 128)) = pack8(kr);
+        *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
+        *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(64 + r, c, 128)) = pack8(qg);
+        *reinterpret_cast<uint4 *>(rec + REC_KT + sw128_offset(r, c, 64)) = pack8(kt);
+        // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a)
+        uint32_t img = P_KC + 2048 * a * (a + 1);   // start of image a
+        *reinterpret_cast<uint4 *>(sm + img + sw128_offset(r, c, 16 * (a + 1))) = pack8(kf);
+#pragma unroll
+        for (int a2 = a + 1; a2 < 4; ++a2) {
+            img = P_KC + 2048 * a2 * (a2 + 1);
+            float rt[8], x[8];
+            ld8(RT + ((a2 * (a2 - 1)) / 2 + a) * DK + c, rt);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) x[i] = kf[i] * rt[i];
+            *reinterpret_cast<uint4 *>(sm + img + sw128_offset(r, c, 16 * (a2 + 1))) = pack8(x);
         }
     }
     fence_proxy_async();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t base = smem_u32(sm);
+
+    // ---- A and P: for each tile a, D_a = [Kr; Qr] x Kc_a^T (M = 128, N = 16(a+1), K = dk)
     if (tid == 0) {
-        tc_fence_after();
-        const uint32_t base = smem_u32(sm);
-        uint32_t img = base + P_KC;
-        for (int a = 0; a < 4; ++a) {
-            const int rows = 16 * (a + 1);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int rows = 16 * (t + 1);
             const uint32_t idesc = idesc_bf16(128, rows, false, false);
-            const uint32_t dcol = 8 * a * (a + 1);
+            const uint32_t img = base + P_KC + 2048 * t * (t + 1);
+            const uint32_t dcol = 8 * t * (t + 1);
             for (int s = 0; s < DK / 16; ++s) {
                 const uint32_t koff = ((s * 16) % 64) * 2;
                 const uint64_t ad = sdesc_sw128(base + P_KRQR + (s >> 2) * 16384 + koff, 16, 1024);
                 const uint64_t bd = sdesc_sw128(img + (s >> 2) * rows * 128 + koff, 16, 1024);
                 umma_bf16(tmem + dcol, ad, bd, idesc, s > 0);
             }
-            img += rows * 256;
         }
         umma_commit(&bar[0]);
     }
-    // K*Gam_C/Gam as the MN-major [64 k-rows][128 m] image (overlaps the MMAs)
-    for (int e = tid; e < C * DK; e += PREP_THREADS) {
-        const int r = e / DK, c = e % DK;
-        st_bf16(sm + P_KT, sw128_offset(r, c, 64), KF[r * DK + c] * RT[(6 + (r >> 4)) * DK + c]);
+    // prefetch this thread's V chunks while the products run
+    uint4 vv[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+        vv[u] = valid ? *reinterpret_cast<const uint4 *>(v + ((t0 + r) * H + h) * (int64_t)DV + 8 * ch)
+                      : make_uint4(0, 0, 0, 0);
     }
     bool ok = mbar_wait(&bar[0], 0);
     tc_fence_after();
 
-    // ---- (3) A and P from TMEM: warp a reads its own lane quarter (tile a)
+    // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+        const int c = 8 * ch;
+        float kk[8], er[8], x[8];
+        unpack8(valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : make_uint4(0, 0, 0, 0), kk);
+        ld8(ER + a * DK + c, er);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) x[i] = kk[i] * (er[i] * __expf(trun[u][i]));  // k_r exp(G_r)
+        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = pack8(x);
+        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c, 64)) = vv[u];
+    }
+    // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
+    // warp t reads its own lane quarter, rows 32t.. of D_t
     float *AS = reinterpret_cast<float *>(sm + P_AS);
     float *TS = reinterpret_cast<float *>(sm + P_TS);
     if (warp < 4) {
-        const int a = warp;
+        const int t = warp;
         const bool isA = lane < 16;
-        const int r = 16 * a + (lane & 15);
-        const float br = BETA[r];
-        const uint32_t dcol = 8 * a * (a + 1);
-        for (int m = 0; m < a + 1; ++m) {
+        const int rr = 16 * t + (lane & 15);
+        const float br = BETA[rr];
+        const uint32_t dcol = 8 * t * (t + 1);
+        for (int m = 0; m < 4; ++m) {
             float val[16];
-            tmem_ld16(tmem + ((uint32_t)(32 * a) << 16) + dcol + 16 * m, val);
-            tmem_ld_wait();
+            if (m <= t) {
+                tmem_ld16(tmem + ((uint32_t)(32 * t) << 16) + dcol + 16 * m, val);
+                tmem_ld_wait();
+            } else {
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int j = 16 * m + i;
-                if (isA) AS[r * 65 + j] = (j < r) ? br * val[i] : 0.f;
-                else st_bf16(sm + P_P, sw128_offset(r, j, 64), (j <= r) ? val[i] : 0.f);
+                for (int i = 0; i < 16; ++i) val[i] = 0.f;
             }
-        }
-        for (int j = 16 * (a + 1); j < C; ++j) {
-            if (isA) AS[r * 65 + j] = 0.f;
-            else st_bf16(sm + P_P, sw128_offset(r, j, 64), 0.f);
+            if (isA) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int j = 16 * m + i;
+                    AS[rr * 65 + j] = (j < rr) ? br * val[i] : 0.f;
+                }
+            } else {
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int j = 16 * m + 8 * half + i;
+                        x[i] = (j <= rr) ? val[8 * half + i] : 0.f;
+                    }
+                    *reinterpret_cast<uint4 *>(rec + REC_P + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
+                }
+            }
         }
     }
     tc_fence_before();
     __syncthreads();
 
-    // ---- (4) T = (I + A)^-1, blocked over 16x16 tiles, fp32
-    if (warp < 4 && lane < 16) {  // diagonal blocks by forward substitution
-        const int a = warp, j = lane;
+    // ---- (D) T = (I + A)^-1 by 16x16 blocks in fp32
+    if (tid < 64) {  // diagonal blocks: thread (block tb, column j) forward-substitutes
+        const int tb = tid >> 4, j = tid & 15;
         float tcol[16];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) {
-            float s = (r == j) ? 1.f : 0.f;
+        for (int i = 0; i < 16; ++i) {
+            float s = (i == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < r; ++m) s -= AS[(16 * a + r) * 65 + 16 * a + m] * tcol[m];
-            tcol[r] = s;
+            for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * 65 + 16 * tb + m] * tcol[m];
+            tcol[i] = s;
         }
 #pragma unroll
-        for (int r = 0; r < 16; ++r) TS[(16 * a + r) * 65 + 16 * a + j] = tcol[r];
+        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * 65 + 16 * tb + j] = tcol[i];
     }
     __syncthreads();
     float *XS = reinterpret_cast<float *>(sm + P_XS);
     for (int d = 1; d < 4; ++d) {
-        // blocks (a, a-d): X = sum_{m=a-d}^{a-1} A_{a,m} T_{m,a-d};  T_{a,a-d} = -T_aa X
-        const int a = d + warp;
-        if (warp < 4 - d) {
-            const int b = a - d;
-            float *X = XS + warp * 16 * 17;
-            for (int e = lane; e < 256; e += 32) {
-                const int i = e >> 4, jj = e & 15;
-                float s = 0.f;
-                for (int m = b; m < a; ++m)
-                    for (int t = 0; t < 16; ++t)
-                        s += AS[(16 * a + i) * 65 + 16 * m + t] * TS[(16 * m + t) * 65 + 16 * b + jj];
-                X[i * 17 + jj] = s;
-            }
-            __syncwarp();
-            for (int e = lane; e < 256; e += 32) {
-                const int i = e >> 4, jj = e & 15;
-                float s = 0.f;
-                for (int t = 0; t <= i; ++t) s += TS[(16 * a + i) * 65 + 16 * a + t] * X[t * 17 + jj];
-                TS[(16 * a + i) * 65 + 16 * b + jj] = -s;
-            }
+        // blocks (a2, a2-d): X = sum_{m=a2-d}^{a2-1} A_{a2,m} T_{m,a2-d};  T_{a2,a2-d} = -T_{a2,a2} X
+        const int nb = 4 - d;
+        for (int e = tid; e < nb * 256; e += PREP_THREADS) {
+            const int bi = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+            const int a2 = d + bi, b = a2 - d;
+            float s = 0.f;
+            for (int m = 16 * b; m < 16 * a2; ++m)
+                s += AS[(16 * a2 + i) * 65 + m] * TS[m * 65 + 16 * b + jj];
+            XS[bi * 272 + i * 17 + jj] = s;
+        }
+        __syncthreads();
+        for (int e = tid; e < nb * 256; e += PREP_THREADS) {
+            const int bi = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+            const int a2 = d + bi, b = a2 - d;
+            float s = 0.f;
+            for (int t = 0; t <= i; ++t) s += TS[(16 * a2 + i) * 65 + 16 * a2 + t] * XS[bi * 272 + t * 17 + jj];
+            TS[(16 * a2 + i) * 65 + 16 * b + jj] = -s;
         }
         __syncthreads();
     }
-    // T diag(b) as the K-major [64][64] A image (upper part zero)
-    for (int e = tid; e < C * C; e += PREP_THREADS) {
-        const int r = e / C, j = e % C;
-        const float x = (j <= r) ? TS[r * 65 + j] * BETA[j] : 0.f;
-        st_bf16(sm + P_TB, sw128_offset(r, j, 64), x);
+    // T diag(b) as the K-major [64][64] A image, 16-byte stores (upper part zero)
+    for (int e = tid; e < C * 8; e += PREP_THREADS) {
+        const int rr = e >> 3, j8 = (e & 7) * 8;
+        float x[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int j = j8 + i;
+            x[i] = (j <= rr) ? TS[rr * 65 + j] * BETA[j] : 0.f;
+        }
+        *reinterpret_cast<uint4 *>(sm + P_TB + sw128_offset(rr, j8, 64)) = pack8(x);
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
-    // ---- (5) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
+    // ---- (E) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
     if (tid == 0) {
         tc_fence_after();
-        const uint32_t base = smem_u32(sm);
         const uint32_t idesc = idesc_bf16(128, 256, false, true);
         for (int s = 0; s < C / 16; ++s) {
             const uint64_t ad = sdesc_sw128(base + P_TB + s * 32, 16, 1024);
@@ -353,19 +408,14 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             umma_bf16(tmem, ad, bd, idesc, s > 0);
         }
         umma_commit(&bar[1]);
-        // the finished images can leave while the MMA runs
-        bulk_s2g(rec + REC_KT, sm + P_KT, 16384);
-        bulk_s2g(rec + REC_P, sm + P_P, 8192);
-        bulk_commit();
     }
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (6) W rows -> WQ image rows 0..63 (warps 0-1); Ut -> fp32 staging (warps 4-5)
-    float *UST = reinterpret_cast<float *>(sm + P_UST);
+    // ---- (F) W rows -> record WQ rows 0..63 (warps 0-1); Ut -> record fp32 (warps 4-5)
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
-        const int quarter = warp & 3;            // TMEM lane quarter 0 or 1
-        const int r = 32 * quarter + lane;       // row of W / Ut
+        const int quarter = warp & 3;
+        const int rr = 32 * quarter + lane;
         const bool isW = warp < 4;
         for (int cb = 0; cb < 4; ++cb) {
             float val[32];
@@ -374,30 +424,21 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             if (isW) {
 #pragma unroll
                 for (int i8 = 0; i8 < 4; ++i8) {
-                    __align__(16) __nv_bfloat16 pk[8];
+                    float x[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) pk[i] = __float2bfloat16_rn(val[8 * i8 + i]);
-                    *reinterpret_cast<uint4 *>(sm + P_WQ + sw128_offset(r, 32 * cb + 8 * i8, 128)) =
-                        *reinterpret_cast<uint4 *>(pk);
+                    for (int i = 0; i < 8; ++i) x[i] = val[8 * i8 + i];
+                    *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(rr, 32 * cb + 8 * i8, 128)) = pack8(x);
                 }
             } else {
-                float4 *dst = reinterpret_cast<float4 *>(UST + (cb * 64 + r) * 32);
+                float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + ((cb * 64 + rr) * 32) * 4);
 #pragma unroll
                 for (int i4 = 0; i4 < 8; ++i4)
                     dst[i4] = make_float4(val[4 * i4], val[4 * i4 + 1], val[4 * i4 + 2], val[4 * i4 + 3]);
             }
         }
     }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-        bulk_s2g(rec + REC_WQ, sm + P_WQ, 32768);
-        bulk_s2g(rec + REC_U, sm + P_UST, 32768);
-        bulk_commit();
-        bulk_wait_all();
-    }
     if (!ok && tid == 0) report(st, KDA_ERR_TIMEOUT, slot, 10);
+    tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();

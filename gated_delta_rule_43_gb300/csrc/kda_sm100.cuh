@@ -167,6 +167,25 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     d |= (uint64_t)2 << 61;  // 128-byte swizzle
     return d;
 }
+// Shared-memory matrix descriptor, 64-byte swizzle (MN-major operands whose MN
+// extent is 32 elements): atoms of 8 rows x 64 bytes, 16-byte chunk index
+// XORed with (row / 2) % 4; SBO = stride of 8-row groups (512 for packed rows).
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo_bytes,
+                                               uint32_t sbo_bytes) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo_bytes >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo_bytes >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;  // version
+    d |= (uint64_t)4 << 61;  // 64-byte swizzle
+    return d;
+}
+// Byte offset of element (k-row r, mn-element m) in an MN-major 64B-swizzled
+// image with 32-element atoms stacked `rows`*64 bytes apart.
+__host__ __device__ __forceinline__ uint32_t sw64_offset(uint32_t r, uint32_t m, uint32_t rows) {
+    return (m / 32) * rows * 64 + r * 64 + ((((m % 32) / 8) ^ ((r >> 1) & 3)) << 4) + (m % 8) * 2;
+}
+
 // Instruction descriptor of kind::f16 with bf16 A and B and an fp32 accumulator.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
                                                   bool b_mn_major) {

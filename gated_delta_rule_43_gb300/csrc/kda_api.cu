@@ -27,7 +27,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
 int64_t chunk_slots(int64_t T_tot, int N, int C);
 cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
                         const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
-                        float *G, StatusWord *st, cudaStream_t s);
+                        int mode, float *G, StatusWord *st, cudaStream_t s);
 }  // namespace kda
 
 using namespace kda;
@@ -243,9 +243,10 @@ kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, 
 
 kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_seqlens,
                            int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
-                           int32_t dtype, int32_t chunk, float *g_cumsum, void *workspace,
-                           size_t workspace_bytes, void *stream) {
+                           int32_t dtype, int32_t chunk, int32_t gate_mode, float *g_cumsum,
+                           void *workspace, size_t workspace_bytes, void *stream) {
     if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
+    if (gate_mode != 0 && gate_mode != 1) return KDA_ERR_INVALID_ARG;
     if (!head_ok(dk)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0 || chunk <= 0 || chunk % kTile != 0)
         return KDA_ERR_INVALID_ARG;
@@ -267,7 +268,7 @@ kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_
     e = launch_plan(cu_seqlens, num_seqs, total_tokens, chunk, chunk_off, st, s);
     if (e != cudaSuccess) return KDA_ERR_CUDA;
     e = launch_gate(dtype, z, A_log, cu_seqlens, chunk_off, num_seqs, total_tokens, H, dk, chunk,
-                    g_cumsum, st, s);
+                    gate_mode, g_cumsum, st, s);
     return cuda_status(e);
 }
 

@@ -29,7 +29,7 @@
 //   WQ  K-major [128 rows][128 K]: rows 0-63 W, rows 64-127 Q*Gam
 //   KT  MN-major [64 k-rows][128 m]: K*Gam_C/Gam, read as the M=dk x K=C operand
 //   P   K-major [64][64]
-//   Ut  fp32 [4 column blocks][64][32]
+//   Ut  fp32 [4 column blocks][64][32], float4 slot j4 of row r holds columns 4 (j4 ^ (r % 8))
 //   GC  fp32 [128] Gam_C
 #include <algorithm>
 
@@ -56,6 +56,7 @@ constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
 constexpr int PREP_THREADS = 256;
+constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and T tiles
 // Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
 // CTAs fit on one SM.  Regions are reused once the A/P products have completed.
 constexpr uint32_t P_BAR = 0;           // 2 mbarriers, TMEM slot
@@ -68,15 +69,15 @@ constexpr uint32_t P_BETA = 12800;      // fp32 [64]
 constexpr uint32_t P_KRQR = 13312;      // K-major [128][128] row-scaled K/Q: tile a -> rows 32a..32a+31
 constexpr uint32_t P_KC = 46080;        // column-scaled K images, a = 0..3: [16(a+1)][128]
 constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64][256]: K*Gam | V
-constexpr uint32_t P_AS = 46080;        //   fp32 A [64][65]
-constexpr uint32_t P_TS = 62720;        //   fp32 T [64][65]
-constexpr uint32_t P_XS = 79360;        //   fp32 [3][16][17] level scratch
+constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
+constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
+constexpr uint32_t P_XS = 80896;        //   fp32 [3][16][16] level scratch
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
 constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
 constexpr uint32_t P_SMEM = P_END + 1024;
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
-static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * 65 * 4 <= P_TS, "prep smem reuse overlaps");
-static_assert(P_TS + 64 * 65 * 4 <= P_XS && P_XS + 3 * 16 * 17 * 4 <= P_TB, "solve scratch");
+static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
+static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 3 * 16 * 16 * 4 <= P_TB, "solve scratch");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
@@ -169,16 +170,32 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     const float expA = expf(A_log[h]);
     if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
 
-    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check
+    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check.
+    //          All of this thread's z, k and q chunks are requested first.
+    uint4 zraw[4], kraw[4], qraw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        zraw[u] = valid ? *reinterpret_cast<const uint4 *>(z + row_off + c) : zero;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
+        qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
+    }
     float trun[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
         float zz[8];
-        unpack8(valid ? *reinterpret_cast<const uint4 *>(z + row_off + 8 * ch) : make_uint4(0, 0, 0, 0), zz);
+        unpack8(zraw[u], zz);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float x = valid ? gate(zz[i], expA) : 0.f;
+            // g = -5 Sigmoid(e^A z) with the fast exponential and divide (bf16 path)
+            float x = valid ? __fdividef(kGMin, 1.0f + __expf(-expA * zz[i])) : 0.f;
 #pragma unroll
             for (int off = 1; off < 16; off <<= 1) {
                 const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
@@ -219,26 +236,30 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr] (smem), column-scaled K
     //          images (smem), Q*Gam and K*Gam_C/Gam (straight into the record)
+    uint4 kgam[4];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
         const int c = 8 * ch;
         float kk[8], qq[8], er[8], ktf[8];
-        unpack8(valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : make_uint4(0, 0, 0, 0), kk);
-        unpack8(valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : make_uint4(0, 0, 0, 0), qq);
+        unpack8(kraw[u], kk);
+        unpack8(qraw[u], qq);
         ld8(ER + a * DK + c, er);
         ld8(KTF + a * DK + c, ktf);
-        float kr[8], qr[8], kf[8], qg[8], kt[8];
+        float kr[8], qr[8], kf[8], qg[8], kt[8], kg[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const float F = __expf(trun[u][i]);       // exp(G_r - ref_a) in [e^-80, 1]
             const float iF = __expf(-trun[u][i]);     // exp(ref_a - G_r) in [1, e^80]
+            const float Gm = er[i] * F;               // exp(G_r)
             kr[i] = kk[i] * F;
             qr[i] = qq[i] * F;
             kf[i] = kk[i] * iF;                       // k_r exp(ref_a - G_r)
-            qg[i] = qq[i] * (er[i] * F);              // q_r exp(G_r)
+            qg[i] = qq[i] * Gm;                       // q_r exp(G_r)
+            kg[i] = kk[i] * Gm;                       // k_r exp(G_r)
             kt[i] = kf[i] * ktf[i];                   // k_r exp(G_C - G_r)
         }
+        kgam[u] = pack8(kg);
         const uint32_t row = 32 * a + rl;
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row, c, 128)) = pack8(kr);
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
@@ -294,14 +315,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
-        const int c = 8 * ch;
-        float kk[8], er[8], x[8];
-        unpack8(valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : make_uint4(0, 0, 0, 0), kk);
-        ld8(ER + a * DK + c, er);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) x[i] = kk[i] * (er[i] * __expf(trun[u][i]));  // k_r exp(G_r)
-        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = pack8(x);
+        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = kgam[u];
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c, 64)) = vv[u];
     }
     // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
@@ -327,7 +342,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     const int j = 16 * m + i;
-                    AS[rr * 65 + j] = (j < rr) ? br * val[i] : 0.f;
+                    AS[rr * LDA + j] = (j < rr) ? br * val[i] : 0.f;
                 }
             } else {
 #pragma unroll
@@ -354,32 +369,43 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         for (int i = 0; i < 16; ++i) {
             float s = (i == j) ? 1.f : 0.f;
 #pragma unroll
-            for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * 65 + 16 * tb + m] * tcol[m];
+            for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * LDA + 16 * tb + m] * tcol[m];
             tcol[i] = s;
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * 65 + 16 * tb + j] = tcol[i];
+        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
     }
     __syncthreads();
     float *XS = reinterpret_cast<float *>(sm + P_XS);
     for (int d = 1; d < 4; ++d) {
         // blocks (a2, a2-d): X = sum_{m=a2-d}^{a2-1} A_{a2,m} T_{m,a2-d};  T_{a2,a2-d} = -T_{a2,a2} X
+        // task = (block, row i, 4-column group jq): 4 outputs per thread
         const int nb = 4 - d;
-        for (int e = tid; e < nb * 256; e += PREP_THREADS) {
-            const int bi = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+        if (tid < nb * 64) {
+            const int bi = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
             const int a2 = d + bi, b = a2 - d;
-            float s = 0.f;
-            for (int m = 16 * b; m < 16 * a2; ++m)
-                s += AS[(16 * a2 + i) * 65 + m] * TS[m * 65 + 16 * b + jj];
-            XS[bi * 272 + i * 17 + jj] = s;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *arow = AS + (16 * a2 + i) * LDA;
+            for (int m = 16 * b; m < 16 * a2; ++m) {
+                const float am = arow[m];
+                const float4 t4 = *reinterpret_cast<const float4 *>(TS + m * LDA + 16 * b + 4 * jq);
+                x.x += am * t4.x; x.y += am * t4.y; x.z += am * t4.z; x.w += am * t4.w;
+            }
+            *reinterpret_cast<float4 *>(XS + bi * 256 + i * 16 + 4 * jq) = x;
         }
         __syncthreads();
-        for (int e = tid; e < nb * 256; e += PREP_THREADS) {
-            const int bi = e >> 8, i = (e >> 4) & 15, jj = e & 15;
+        if (tid < nb * 64) {
+            const int bi = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
             const int a2 = d + bi, b = a2 - d;
-            float s = 0.f;
-            for (int t = 0; t <= i; ++t) s += TS[(16 * a2 + i) * 65 + 16 * a2 + t] * XS[bi * 272 + t * 17 + jj];
-            TS[(16 * a2 + i) * 65 + 16 * b + jj] = -s;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            const float *trow = TS + (16 * a2 + i) * LDA + 16 * a2;
+            for (int t = 0; t <= i; ++t) {
+                const float tt = trow[t];
+                const float4 x4 = *reinterpret_cast<const float4 *>(XS + bi * 256 + t * 16 + 4 * jq);
+                x.x += tt * x4.x; x.y += tt * x4.y; x.z += tt * x4.z; x.w += tt * x4.w;
+            }
+            *reinterpret_cast<float4 *>(TS + (16 * a2 + i) * LDA + 16 * b + 4 * jq) =
+                make_float4(-x.x, -x.y, -x.z, -x.w);
         }
         __syncthreads();
     }
@@ -390,7 +416,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int j = j8 + i;
-            x[i] = (j <= rr) ? TS[rr * 65 + j] * BETA[j] : 0.f;
+            x[i] = (j <= rr) ? TS[rr * LDA + j] * BETA[j] : 0.f;
         }
         *reinterpret_cast<uint4 *>(sm + P_TB + sw128_offset(rr, j8, 64)) = pack8(x);
     }
@@ -430,10 +456,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                     *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(rr, 32 * cb + 8 * i8, 128)) = pack8(x);
                 }
             } else {
+                // row rr of column block cb; float4 j4 stored at slot j4 ^ (rr % 8) so that the
+                // chain kernel's row-per-thread reads hit distinct banks
                 float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + ((cb * 64 + rr) * 32) * 4);
 #pragma unroll
                 for (int i4 = 0; i4 < 8; ++i4)
-                    dst[i4] = make_float4(val[4 * i4], val[4 * i4 + 1], val[4 * i4 + 2], val[4 * i4 + 3]);
+                    dst[i4 ^ (rr & 7)] = make_float4(val[4 * i4], val[4 * i4 + 1], val[4 * i4 + 2], val[4 * i4 + 3]);
             }
         }
     }
@@ -450,12 +478,13 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 constexpr int CHAIN_THREADS = 128;
 constexpr uint32_t B_WQ = 0, B_KT = 32768, B_ZP = 49152, B_U = 65536, B_G = 73728;
 constexpr uint32_t BUF_BYTES = 74752;
-constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image K-major [32][128]
-constexpr uint32_t C_UI = C_S + 8192;                // U image K-major [32][64]
-constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, TMEM slot
+constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
+constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
+constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, TMEM slot, abort flag
 constexpr uint32_t C_SMEM = C_BAR + 64 + 1024;
 constexpr uint32_t LOAD_BYTES = 32768 + 16384 + 8192 + 8192 + 512;
 static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0, "chain buffer layout");
+static_assert(C_S % 1024 == 0 && C_UI % 1024 == 0, "operand image alignment");
 static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int blk,
@@ -478,10 +507,25 @@ __device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32
     return lo;
 }
 
+// 32 fp32 values -> four 16-byte chunks of row r of a 64B-swizzled MN-major image
+__device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float (&x)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = x[8 * c8 + i];
+        *reinterpret_cast<uint4 *>(img + sw64_offset(r, 8 * c8, 1)) = pack8(y);
+    }
+}
+
 // Persistent over work items (sequence, head, 32-column block) of the sequences
-// that own chunks in the slot window [slot0, slot1); each item walks its
-// chunks in order, carrying its block of S in registers (fp32) and as the bf16
-// B operand image in shared memory.
+// that own chunks in the slot window [slot0, slot1); each item walks its chunks
+// in order, carrying its block of S in registers (fp32, thread i = row i) and as
+// the bf16 B operand image.  Per chunk, on the critical path:
+//   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
+//   D1 += [0; P] U     ->  S = Diag(Gam_C) S + D2.
+// D1 is double-buffered in TMEM so that the output rows of chunk c (D1[64:128])
+// are stored by warps 2-3 while warps 0-1 form U of chunk c+1.
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
@@ -510,17 +554,18 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         reinterpret_cast<uint4 *>(b)[e % 512] = make_uint4(0, 0, 0, 0);
     }
     if (warp == 0) {
-        tmem_alloc(tslot, 64);
+        tmem_alloc(tslot, 128);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const uint32_t D1 = tmem, D2 = tmem + 32;
+    const uint32_t D2 = tmem + 64;                     // D1 buffers at columns 0 and 32
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const uint32_t base = smem_u32(sm);
-    const uint32_t id_kk = idesc_bf16(128, DVB, false, false);
-    const uint32_t id_mk = idesc_bf16(128, DVB, true, false);
+    const uint32_t id_km = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
+    const uint32_t id_mm = idesc_bf16(128, DVB, true, true);    // A MN-major, B MN-major
     const int i = tid;  // this thread's state row
     uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
@@ -528,7 +573,8 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         const int blk = item % NBLK;
         const int h = (item / NBLK) % H;
         const int n = n_first + item / (NBLK * H);
-        const int32_t c_begin = max(chunk_off[n], slot0);
+        const int32_t cfirst = chunk_off[n];
+        const int32_t c_begin = max(cfirst, slot0);
         const int32_t c_end = min(chunk_off[n + 1], slot1);
         if (c_begin >= c_end) continue;
         const int64_t bos = cu[n];
@@ -541,8 +587,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
             S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
         }
-#pragma unroll
-        for (int j = 0; j < DVB; ++j) st_bf16(sm + C_S, sw128_offset(j, i, 32), S[j]);
+        store_row_sw64(sm + C_S, i, S);
         fence_proxy_async();
         __syncthreads();
         if (tid == 0)
@@ -550,19 +595,38 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                        records + ((size_t)(c_begin - slot0) * H + h) * REC_BYTES, blk,
                        &bar[gi & 1]);
 
+        // output rows of the chunk whose D1 buffer is `pb` (warps 2-3)
+        auto store_o = [&](int32_t cprev, uint32_t pb) {
+            const int r = tid - 64;
+            const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
+            float oacc[32];
+            tmem_ld32(tmem + 32 * pb + lane_base, oacc);
+            tmem_ld_wait();
+            if (t < eos) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8) {
+                    float y[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) y[x] = oacc[8 * i8 + x];
+                    dst[i8] = pack8(y);
+                }
+            }
+        };
+
         for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
             const uint32_t b = gi & 1;
             uint8_t *buf = sm + b * BUF_BYTES;
             const uint32_t bufa = base + b * BUF_BYTES;
             bool ok = mbar_wait(&bar[b], (gi >> 1) & 1);
             if (tid == 0 && ok) {
-                // D1 = [W; Q*Gam] S
+                // D1[b] = [W; Q*Gam] S
                 tc_fence_after();
                 for (int s = 0; s < DK / 16; ++s) {
                     const uint32_t koff = ((s * 16) % 64) * 2;
                     const uint64_t ad = sdesc_sw128(bufa + B_WQ + (s >> 2) * 16384 + koff, 16, 1024);
-                    const uint64_t bd = sdesc_sw128(base + C_S + (s >> 2) * 4096 + koff, 16, 1024);
-                    umma_bf16(D1, ad, bd, id_kk, s > 0);
+                    const uint64_t bd = sdesc_sw64(base + C_S + s * 1024, 128 * 64, 512);
+                    umma_bf16(tmem + 32 * b, ad, bd, id_km, s > 0);
                 }
                 umma_commit(&bar[2]);
                 // prefetch the next chunk into the other buffer (its last reader finished)
@@ -571,23 +635,28 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                                records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
                                &bar[b ^ 1]);
             }
-            ok = ok && mbar_wait(&bar[2], gi & 1);
-            tc_fence_after();
-            // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
-            if (warp < 2 && ok) {
-                const int r = tid;
-                float acc[32];
-                tmem_ld32(D1 + ((uint32_t)(32 * warp) << 16), acc);
-                tmem_ld_wait();
-                const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
+            if (warp < 2) {
+                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
+                ok = ok && mbar_wait(&bar[2], gi & 1);
+                tc_fence_after();
+                if (ok) {
+                    const int r = tid;
+                    float acc[32];
+                    tmem_ld32(tmem + 32 * b + lane_base, acc);
+                    tmem_ld_wait();
+                    const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) {
-                    const float4 u4 = ut[j4];
-                    st_bf16(sm + C_UI, sw128_offset(4 * j4 + 0, r, 32), u4.x - acc[4 * j4 + 0]);
-                    st_bf16(sm + C_UI, sw128_offset(4 * j4 + 1, r, 32), u4.y - acc[4 * j4 + 1]);
-                    st_bf16(sm + C_UI, sw128_offset(4 * j4 + 2, r, 32), u4.z - acc[4 * j4 + 2]);
-                    st_bf16(sm + C_UI, sw128_offset(4 * j4 + 3, r, 32), u4.w - acc[4 * j4 + 3]);
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 u4 = ut[j4 ^ (r & 7)];
+                        acc[4 * j4 + 0] = u4.x - acc[4 * j4 + 0];
+                        acc[4 * j4 + 1] = u4.y - acc[4 * j4 + 1];
+                        acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
+                        acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
+                    }
+                    store_row_sw64(sm + C_UI, r, acc);
                 }
+            } else if (cs > c_begin) {
+                store_o(cs - 1, b ^ 1);   // previous chunk's outputs, off the critical path
             }
             if (!ok) *abort_flag = 1;
             fence_proxy_async();
@@ -597,12 +666,12 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             if (tid == 0) {
                 tc_fence_after();
                 for (int s = 0; s < C / 16; ++s) {
-                    // D2 = (K*Gam_C/Gam)^T U ;  D1 += [0; P] U
-                    const uint64_t bd = sdesc_sw128(base + C_UI + s * 32, 16, 1024);
+                    // D2 = (K*Gam_C/Gam)^T U ;  D1[b] += [0; P] U
+                    const uint64_t bd = sdesc_sw64(base + C_UI + s * 1024, 64 * 64, 512);
                     const uint64_t akt = sdesc_sw128(bufa + B_KT + s * 2048, 64 * 128, 1024);
-                    umma_bf16(D2, akt, bd, id_mk, s > 0);
+                    umma_bf16(D2, akt, bd, id_mm, s > 0);
                     const uint64_t azp = sdesc_sw128(bufa + B_ZP + s * 32, 16, 1024);
-                    umma_bf16(D1, azp, bd, id_kk, 1);
+                    umma_bf16(tmem + 32 * b, azp, bd, id_km, 1);
                 }
                 umma_commit(&bar[3]);
             }
@@ -612,31 +681,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 // S <- Diag(Gam_C) S + D2 (row i = tid)
                 const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
                 float acc[32];
-                tmem_ld32(D2 + ((uint32_t)(32 * warp) << 16), acc);
+                tmem_ld32(D2 + lane_base, acc);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < DVB; ++j) {
-                    S[j] = gc * S[j] + acc[j];
-                    st_bf16(sm + C_S, sw128_offset(j, i, 32), S[j]);
-                }
-                if (warp >= 2) {
-                    // O rows live in TMEM lane quarters 2 and 3 of D1
-                    const int r = tid - 64;
-                    const int64_t t = bos + (int64_t)(cs - chunk_off[n]) * C + r;
-                    float oacc[32];
-                    tmem_ld32(D1 + ((uint32_t)(32 * warp) << 16), oacc);
-                    tmem_ld_wait();
-                    if (t < eos) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
-#pragma unroll
-                        for (int i8 = 0; i8 < 4; ++i8) {
-                            __align__(16) __nv_bfloat16 pk[8];
-#pragma unroll
-                            for (int x = 0; x < 8; ++x) pk[x] = __float2bfloat16_rn(oacc[8 * i8 + x]);
-                            dst[i8] = *reinterpret_cast<uint4 *>(pk);
-                        }
-                    }
-                }
+                for (int j = 0; j < DVB; ++j) S[j] = gc * S[j] + acc[j];
+                store_row_sw64(sm + C_S, i, S);
             } else {
                 *abort_flag = 1;
             }
@@ -648,17 +697,20 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         if (*abort_flag) {
             if (tid == 0) report(st, KDA_ERR_TIMEOUT, ((int64_t)n * H + h) * NBLK + blk, 11);
         } else {
+            tc_fence_after();
+            if (warp >= 2) store_o(c_end - 1, (gi - 1) & 1);   // the item's last chunk
 #pragma unroll
             for (int j4 = 0; j4 < DVB / 4; ++j4)
                 reinterpret_cast<float4 *>(srow)[j4] =
                     make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
         }
+        tc_fence_before();
         __syncthreads();
     }
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, 64);
+        tmem_dealloc(tmem, 128);
     }
 }
 

@@ -73,12 +73,20 @@ __device__ __forceinline__ int find_seq(const int32_t *chunk_off, int N, int32_t
     return lo;
 }
 
+// The unbounded baseline the lower-bounded gate replaces (same section of the
+// dev.to page: "replaces unbounded negative Softplus decay"): g = -Softplus(e^A z).
+__device__ __forceinline__ float gate_softplus(float z, float expA) {
+    const float x = expA * z;
+    return x > 40.f ? -x : -log1pf(expf(x));
+}
+
 // One CTA per (chunk slot, head); thread c walks channel c of the chunk.
+// mode 0: the lower-bounded gate; mode 1: the Softplus baseline.
 template <typename T>
 __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restrict__ A_log,
                                    const int32_t *__restrict__ cu,
                                    const int32_t *__restrict__ chunk_off, int N, int H, int dk,
-                                   int C, float *__restrict__ G, StatusWord *st) {
+                                   int C, int mode, float *__restrict__ G, StatusWord *st) {
     const int32_t slot = blockIdx.x;
     const int h = blockIdx.y;
     const int n = find_seq(chunk_off, N, slot);
@@ -90,7 +98,8 @@ __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restr
         float run = 0.f, tile = 0.f;
         for (int64_t t = t0; t < t1; ++t) {
             const int64_t idx = (t * H + h) * (int64_t)dk + c;
-            const float g = gate(to_f(z[idx]), expA);
+            const float zz = to_f(z[idx]);
+            const float g = mode == 1 ? gate_softplus(zz, expA) : gate(zz, expA);
             if (((t - t0) % kTile) == 0) tile = 0.f;
             run += g;
             tile += g;
@@ -110,16 +119,16 @@ int64_t chunk_slots(int64_t T_tot, int N, int C) { return (T_tot + C - 1) / C + 
 
 cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
                         const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
-                        float *G, StatusWord *st, cudaStream_t s) {
+                        int mode, float *G, StatusWord *st, cudaStream_t s) {
     const int64_t slots = chunk_slots(T_tot, N, C);
     if (slots <= 0) return cudaSuccess;
     dim3 grid((unsigned)slots, (unsigned)H);
     if (dtype == KDA_BF16)
         gate_cumsum_kernel<__nv_bfloat16><<<grid, dk, 0, s>>>(
-            (const __nv_bfloat16 *)z, A_log, cu, chunk_off, N, H, dk, C, G, st);
+            (const __nv_bfloat16 *)z, A_log, cu, chunk_off, N, H, dk, C, mode, G, st);
     else
         gate_cumsum_kernel<float><<<grid, dk, 0, s>>>((const float *)z, A_log, cu, chunk_off, N,
-                                                      H, dk, C, G, st);
+                                                      H, dk, C, mode, G, st);
     return cudaGetLastError();
 }
 

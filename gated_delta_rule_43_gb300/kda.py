@@ -38,7 +38,7 @@ SIGNATURES = {
     "kda_decode_step": (I32, [P, P, P, P, P, P, P, P, I32, I32, I32, I32, I32, P, SZ, P]),
     "kda_decode_step_indexed": (I32, [P, P, P, P, P, P, P, P, I32, P, I32, I32, I32, I32, I32, P,
                                       SZ, P]),
-    "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, P, P, SZ, P]),
+    "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, SZ, P]),
     "kda_query_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int64)]),
 }
 
@@ -247,9 +247,12 @@ def decode_step_indexed(q, k, v, z, beta, A_log, state_pool, state_idx, *, o=Non
     return o
 
 
-def gate_cumsum(z, A_log, cu_seqlens, chunk: int = 64, *, workspace=None, stream=None,
-                check: bool = False):
-    """The standalone gate kernel (kda_gate_cumsum): fp32 in-chunk cumsum of g [T, H, dk]."""
+def gate_cumsum(z, A_log, cu_seqlens, chunk: int = 64, *, softplus: bool = False,
+                workspace=None, stream=None, check: bool = False):
+    """The standalone gate kernel (kda_gate_cumsum): fp32 in-chunk cumsum of g [T, H, dk].
+
+    softplus=True evaluates the unbounded -Softplus baseline instead of the
+    lower-bounded gate (same 16-token range check)."""
     lib = load()
     _check_cuda(z, A_log, cu_seqlens, workspace)
     T, H, dk = z.shape
@@ -260,7 +263,8 @@ def gate_cumsum(z, A_log, cu_seqlens, chunk: int = 64, *, workspace=None, stream
         workspace = alloc_workspace(int(lib.kda_chunk_fwd_workspace_size(T, N, H, dk, dk, dt)),
                                     z.device)
     rc = lib.kda_gate_cumsum(_ptr(z), _ptr(A_log), _ptr(cu_seqlens), N, T, H, dk, dt, chunk,
-                             _ptr(G), _ptr(workspace), workspace.numel(), _stream(stream))
+                             1 if softplus else 0, _ptr(G), _ptr(workspace), workspace.numel(),
+                             _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_gate_cumsum")
     if check:

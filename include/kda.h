@@ -224,12 +224,16 @@ kda_status kda_decode_step_indexed(const void *q, const void *k, const void *v, 
  * equation) and records KDA_ERR_DECAY_RANGE on a violation.  `chunk` must
  * be a positive multiple of 16.  kda_chunk_fwd fuses the same computation
  * into its own kernels; this entry exposes it for inspection.
+ * gate_mode 0 is the lower-bounded gate above; gate_mode 1 evaluates the
+ * unbounded baseline the page says it replaces, g = -Softplus(exp(A_h) z),
+ * with the same range check, for an A/B of the bound (the chunked forward
+ * accepts only the bounded gate).
  * Workspace: >= kda_chunk_fwd_workspace_size(total_tokens, num_seqs, H, dk, dk, dtype).
  */
 kda_status kda_gate_cumsum(const void *z, const float *A_log, const int32_t *cu_seqlens,
                            int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
-                           int32_t dtype, int32_t chunk, float *g_cumsum, void *workspace,
-                           size_t workspace_bytes, void *stream);
+                           int32_t dtype, int32_t chunk, int32_t gate_mode, float *g_cumsum,
+                           void *workspace, size_t workspace_bytes, void *stream);
 
 /*
  * Waits for `stream`, then returns the status recorded in `workspace` by the

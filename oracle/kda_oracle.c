@@ -65,6 +65,17 @@ static double gate(double z, double A, double g_min) {
     return g_min / (1.0 + exp(-x));
 }
 
+/*
+ * The unbounded baseline the lower-bounded gate replaces ("Kimi K3
+ * Architecture...", section "The Sequence Bottleneck": "replaces unbounded
+ * negative Softplus decay"): g = -Softplus(exp(A) * z), Softplus(x) =
+ * log(1 + exp(x)), read with the same argument as the bounded gate.
+ */
+static double gate_softplus(double z, double A) {
+    double x = exp(A) * z;
+    return x > 40.0 ? -x : -log1p(exp(x));
+}
+
 int kda_oracle_threads(void) {
 #ifdef _OPENMP
     return omp_get_max_threads();
@@ -75,6 +86,7 @@ int kda_oracle_threads(void) {
 
 /*
  * Gate and in-tile cumulative decay.
+ *   mode   0: the lower-bounded gate; 1: the Softplus baseline
  *   z      [T_tot, H, dk] in dtype dt
  *   A_log  [H] (the per-head A^h)
  *   g_out  [T_tot, H, dk] fp64 (may be NULL)
@@ -86,7 +98,7 @@ int kda_oracle_threads(void) {
  */
 int64_t kda_oracle_gate(const void *z, int dt, const double *A_log, const int64_t *cu_seqlens,
                         int32_t N, int32_t H, int32_t dk, int32_t tile, double g_min,
-                        double *g_out, double *G_out) {
+                        int mode, double *g_out, double *G_out) {
     int64_t bad = 0;
     for (int32_t n = 0; n < N; ++n) {
         for (int32_t h = 0; h < H; ++h) {
@@ -95,7 +107,8 @@ int64_t kda_oracle_gate(const void *z, int dt, const double *A_log, const int64_
                 for (int64_t t = cu_seqlens[n]; t < cu_seqlens[n + 1]; ++t) {
                     if ((t - cu_seqlens[n]) % tile == 0) run = 0.0;
                     int64_t idx = (t * H + h) * (int64_t)dk + c;
-                    double g = gate(ld(z, dt, idx), A_log[h], g_min);
+                    double g = mode == 1 ? gate_softplus(ld(z, dt, idx), A_log[h])
+                                         : gate(ld(z, dt, idx), A_log[h], g_min);
                     run += g;
                     if (g_out) g_out[idx] = g;
                     if (G_out) G_out[idx] = run;

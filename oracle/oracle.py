@@ -53,7 +53,7 @@ def _bind(path: str):
     P, I32, I64, D, I = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double,
                          ctypes.c_int)
     lib.kda_oracle_gate.restype = I64
-    lib.kda_oracle_gate.argtypes = [P, I, P, P, I32, I32, I32, I32, D, P, P]
+    lib.kda_oracle_gate.argtypes = [P, I, P, P, I32, I32, I32, I32, D, I, P, P]
     lib.kda_oracle_forward.restype = I
     lib.kda_oracle_forward.argtypes = [P, P, P, P, P, I, P, P, I32, I32, I32, I32, P, P, P, P, I,
                                        P, I32, D, I]
@@ -104,11 +104,13 @@ class Oracle:
         self.lib.kda_oracle_widen(a.ctypes.data, _code(a), a.size, out.ctypes.data)
         return out
 
-    def gate(self, z, A_log, cu_seqlens, tile: int = 16, g_min: float = G_MIN):
+    def gate(self, z, A_log, cu_seqlens, tile: int = 16, g_min: float = G_MIN,
+             softplus: bool = False):
         """g = g_min*Sigmoid(exp(A_h) z) and its in-tile inclusive cumsum.
 
-        Returns (g, G, bad): fp64 arrays shaped like z and the number of tile
-        prefix sums outside [-80, 0] or not finite.
+        softplus=True evaluates the unbounded baseline g = -Softplus(exp(A_h) z)
+        instead.  Returns (g, G, bad): fp64 arrays shaped like z and the number
+        of tile prefix sums outside [-80, 0] or not finite.
         """
         z = np.ascontiguousarray(z)
         T, H, dk = z.shape
@@ -117,8 +119,8 @@ class Oracle:
         g = np.empty(z.shape, np.float64)
         G = np.empty(z.shape, np.float64)
         bad = self.lib.kda_oracle_gate(z.ctypes.data, _code(z), A.ctypes.data, cu.ctypes.data,
-                                       len(cu) - 1, H, dk, tile, g_min, g.ctypes.data,
-                                       G.ctypes.data)
+                                       len(cu) - 1, H, dk, tile, g_min, 1 if softplus else 0,
+                                       g.ctypes.data, G.ctypes.data)
         return g, G, int(bad)
 
     def forward(self, q, k, v, z, beta, A_log, cu_seqlens, h0=None, *, want_o=True,

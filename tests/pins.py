@@ -101,6 +101,25 @@ def pin_tile_cumsum(orc):
     assert badn > 0, "NaN must be flagged"
 
 
+def pin_softplus_baseline(orc):
+    """The unbounded baseline: -Softplus(0) = -ln 2, -> 0 for large negative arguments,
+    -> -x for large positive ones; below g_min where the bounded gate saturates."""
+    z = np.array([[[0.0, -60.0, 50.0, 10.0, 2.0]]])
+    g, _, _ = orc.gate(z, [0.0], [0, 1], softplus=True)
+    g = g[0, 0]
+    assert abs(g[0] + math.log(2.0)) < 1e-15
+    assert -1e-25 < g[1] < 0.0
+    assert g[2] == -50.0
+    assert abs(g[3] + (10.0 + math.log1p(math.exp(-10.0)))) < 1e-12
+    assert abs(g[4] + math.log1p(math.exp(2.0))) < 1e-14
+    # 16 tokens at z = 10 leave the bounded gate at the -80 edge and the baseline far below it
+    zt = np.full((16, 1, 1), 10.0)
+    _, Gb, bad_b = orc.gate(zt, [0.0], [0, 16])
+    _, Gs, bad_s = orc.gate(zt, [0.0], [0, 16], softplus=True)
+    assert bad_b == 0 and Gb[-1, 0, 0] >= -80.0
+    assert bad_s > 0 and Gs[-1, 0, 0] < -160.0
+
+
 # ---------------------------------------------------------------- recurrence
 
 def pin_single_step(orc):
@@ -291,7 +310,8 @@ def pin_score_sums(orc):
             assert abs(sc["ref2"][n, h] - r2) <= 1e-12 * r2
 
 
-PINS = [pin_gate_closed_forms, pin_gate_bounds, pin_tile_cumsum, pin_single_step,
+PINS = [pin_gate_closed_forms, pin_gate_bounds, pin_tile_cumsum, pin_softplus_baseline,
+        pin_single_step,
         pin_dense_bruteforce, pin_noop, pin_pure_decay, pin_householder, pin_contraction,
         pin_split_resume, pin_varlen_independence, pin_decode_matches_prefill,
         pin_chunk_algebra, pin_column_blocks, pin_bf16_reader, pin_score_sums]

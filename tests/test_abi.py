@@ -106,15 +106,16 @@ def test_argument_validation_returns_before_launch(lib):
 
     def gate(**kw):
         args = dict(z=p[0], A=p[1], cu=p[2], N=1, T=64, H=2, dk=32, dt=kda.KDA_F32, C=64,
-                    G=p[3], ws=p[4], wsb=ws_need)
+                    mode=0, G=p[3], ws=p[4], wsb=ws_need)
         args.update(kw)
         return lib.kda_gate_cumsum(args["z"], args["A"], args["cu"], args["N"], args["T"],
-                                   args["H"], args["dk"], args["dt"], args["C"], args["G"],
-                                   args["ws"], args["wsb"], None)
+                                   args["H"], args["dk"], args["dt"], args["C"], args["mode"],
+                                   args["G"], args["ws"], args["wsb"], None)
 
     assert gate(C=24) == kda.KDA_ERR_INVALID_ARG                   # not a multiple of 16
     assert gate(dk=16) == kda.KDA_ERR_UNSUPPORTED
     assert gate(G=p[0]) == kda.KDA_ERR_INVALID_ARG                 # output aliases z
+    assert gate(mode=2) == kda.KDA_ERR_INVALID_ARG                 # unknown gate mode
     assert lib.kda_query_status(None, None, None) == kda.KDA_ERR_INVALID_ARG
 
 

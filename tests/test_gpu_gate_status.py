@@ -52,3 +52,24 @@ def test_bad_cu_seqlens_are_reported():
     o, s = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
                          d["cu_seqlens"], check=True)
     assert torch.isfinite(o).all()
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_softplus_baseline_gate_and_the_bound(dtype):
+    """A/B of the lower bound: on the same z, the unbounded -Softplus gate pushes 16-token
+    tile sums below -80 (flagged) while the bounded gate stays inside [-80, 0]."""
+    d = inputs.make_prefill([100, 37], H=2, dk=32, dv=32, dtype=dtype, seed=21, device=DEV)
+    d["z"][:16] = 20.0         # strong gates on the first tile of sequence 0
+    host_z = inputs.host_array(d["z"])
+    A = d["A_log"].cpu().numpy()
+    cu = d["cu_seqlens"].cpu().numpy()
+    Gs, _ = kda.gate_cumsum(d["z"], d["A_log"], d["cu_seqlens"], chunk=16, softplus=True)
+    code, _ = kda.query_status(_)
+    _, Gs_ref, bad_s = orc.gate(host_z, A, cu, tile=16, softplus=True)
+    assert bad_s > 0 and code == kda.KDA_ERR_DECAY_RANGE
+    err = np.abs(Gs.cpu().numpy().astype(np.float64) - Gs_ref)
+    assert float(err.max()) <= 1e-5 * max(1.0, float(np.abs(Gs_ref).max()))
+    Gb, wsb = kda.gate_cumsum(d["z"], d["A_log"], d["cu_seqlens"], chunk=16, check=True)
+    _, Gb_ref, bad_b = orc.gate(host_z, A, cu, tile=16)
+    assert bad_b == 0
+    assert float(Gb.min()) >= -80.0

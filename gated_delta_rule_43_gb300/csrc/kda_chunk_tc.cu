@@ -71,13 +71,13 @@ constexpr uint32_t P_KC = 46080;        // column-scaled K images, a = 0..3: [16
 constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64][256]: K*Gam | V
 constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
-constexpr uint32_t P_XS = 80896;        //   fp32 [3][16][16] level scratch
+constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
 constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
 constexpr uint32_t P_SMEM = P_END + 1024;
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
-static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 3 * 16 * 16 * 4 <= P_TB, "solve scratch");
+static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
@@ -151,27 +151,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_BAR + 16);
 
-    if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        fence_mbar_init();
-    }
-    if (warp == 0) {
-        tmem_alloc(tslot, 256);
-        tmem_relinquish();
-        tc_fence_before();
-    }
-
     const int a = warp & 3;                    // this thread's 16-token tile
     const int rl = lane & 15;
     const int r = 16 * a + rl;                 // this thread's row of the chunk
     const bool valid = r < L;
     const int64_t row_off = ((t0 + r) * H + h) * (int64_t)DK;
-    const float expA = expf(A_log[h]);
-    if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
-
-    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check.
-    //          All of this thread's z, k and q chunks are requested first.
+    // All of this thread's z, k and q chunks are requested before any set-up.
     uint4 zraw[4], kraw[4], qraw[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -186,6 +171,20 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
         qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
     }
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 256);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    const float expA = expf(A_log[h]);
+    if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
+
+    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check
     float trun[4][8];
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -361,8 +360,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     tc_fence_before();
     __syncthreads();
 
-    // ---- (D) T = (I + A)^-1 by 16x16 blocks in fp32
-    if (tid < 64) {  // diagonal blocks: thread (block tb, column j) forward-substitutes
+    // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
+    //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
+    //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
+    if (tid < 64) {  // diagonal blocks T_aa = (I + A_aa)^-1: thread (block tb, column j)
         const int tb = tid >> 4, j = tid & 15;
         float tcol[16];
 #pragma unroll
@@ -376,39 +377,94 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
     }
     __syncthreads();
-    float *XS = reinterpret_cast<float *>(sm + P_XS);
-    for (int d = 1; d < 4; ++d) {
-        // blocks (a2, a2-d): X = sum_{m=a2-d}^{a2-1} A_{a2,m} T_{m,a2-d};  T_{a2,a2-d} = -T_{a2,a2} X
-        // task = (block, row i, 4-column group jq): 4 outputs per thread
-        const int nb = 4 - d;
-        if (tid < nb * 64) {
-            const int bi = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
-            const int a2 = d + bi, b = a2 - d;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *arow = AS + (16 * a2 + i) * LDA;
-            for (int m = 16 * b; m < 16 * a2; ++m) {
-                const float am = arow[m];
-                const float4 t4 = *reinterpret_cast<const float4 *>(TS + m * LDA + 16 * b + 4 * jq);
-                x.x += am * t4.x; x.y += am * t4.y; x.z += am * t4.z; x.w += am * t4.w;
+    // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
+    // The diagonal blocks of T hold explicit zeros above the diagonal, so every product
+    // below runs over all 16 terms (fixed trip counts, fully unrolled).
+    auto pair_a = [](int pr) { return pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3); };
+    auto pair_b = [](int pr) { return pr < 3 ? pr : (pr == 4 ? 1 : 0); };
+    // dst += X[16 x 16 block rows] (row i) times Y (16 x 4 column group)
+    auto acc16 = [](float4 &x, const float *xrow, const float *ycol, int ystride) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const float xv = xrow[t];
+            const float4 y = *reinterpret_cast<const float4 *>(ycol + t * ystride);
+            x.x += xv * y.x; x.y += xv * y.y; x.z += xv * y.z; x.w += xv * y.w;
+        }
+    };
+    // N_ab = T_aa A_ab, in place over A (all reads happen before the barrier)
+    {
+        float4 nv[2];
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
+            nv[w] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (task < 384) {
+                const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
+                const int a2 = pair_a(pr), b = pair_b(pr);
+                acc16(nv[w], TS + (16 * a2 + i) * LDA + 16 * a2, AS + (16 * a2) * LDA + 16 * b + 4 * jq, LDA);
             }
-            *reinterpret_cast<float4 *>(XS + bi * 256 + i * 16 + 4 * jq) = x;
         }
         __syncthreads();
-        if (tid < nb * 64) {
-            const int bi = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
-            const int a2 = d + bi, b = a2 - d;
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            const float *trow = TS + (16 * a2 + i) * LDA + 16 * a2;
-            for (int t = 0; t <= i; ++t) {
-                const float tt = trow[t];
-                const float4 x4 = *reinterpret_cast<const float4 *>(XS + bi * 256 + t * 16 + 4 * jq);
-                x.x += tt * x4.x; x.y += tt * x4.y; x.z += tt * x4.z; x.w += tt * x4.w;
+#pragma unroll
+        for (int w = 0; w < 2; ++w) {
+            const int task = tid + w * PREP_THREADS;
+            if (task < 384) {
+                const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
+                *reinterpret_cast<float4 *>(AS + (16 * pair_a(pr) + i) * LDA + 16 * pair_b(pr) + 4 * jq) = nv[w];
             }
-            *reinterpret_cast<float4 *>(TS + (16 * a2 + i) * LDA + 16 * b + 4 * jq) =
-                make_float4(-x.x, -x.y, -x.z, -x.w);
         }
-        __syncthreads();
     }
+    __syncthreads();
+    float *XS = reinterpret_cast<float *>(sm + P_XS);   // [0] N2_20 [1] N2_31 [2] N2_30 [3] N3_30
+    auto nrow = [&](int a2, int b, int i) { return AS + (16 * a2 + i) * LDA + 16 * b; };
+    if (tid < 192) {
+        // N^2 blocks: (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20 (warp-uniform q)
+        const int q = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (q == 0) {
+            acc16(x, nrow(2, 1, i), AS + 16 * LDA + 4 * jq, LDA);
+        } else if (q == 1) {
+            acc16(x, nrow(3, 2, i), AS + 32 * LDA + 16 + 4 * jq, LDA);
+        } else {
+            acc16(x, nrow(3, 1, i), AS + 16 * LDA + 4 * jq, LDA);
+            acc16(x, nrow(3, 2, i), AS + 32 * LDA + 4 * jq, LDA);
+        }
+        *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
+    }
+    __syncthreads();
+    if (tid < 64) {  // N^3_30 = N32 N^2_20
+        const int i = tid >> 2, jq = tid & 3;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        acc16(x, nrow(3, 2, i), XS + 4 * jq, 16);
+        *reinterpret_cast<float4 *>(XS + 3 * 256 + i * 16 + 4 * jq) = x;
+    }
+    __syncthreads();
+    // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise)
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const int task = tid + w * PREP_THREADS;
+        if (task < 384) {
+            const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
+            const int a2 = pair_a(pr), b = pair_b(pr);
+            const int n2 = pr == 3 ? 0 : pr == 4 ? 1 : pr == 5 ? 2 : -1;
+            float mrow[16];
+            const float *nr = nrow(a2, b, i);
+#pragma unroll
+            for (int t = 0; t < 16; ++t) mrow[t] = -nr[t];
+            if (n2 >= 0) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) mrow[t] += XS[n2 * 256 + i * 16 + t];
+            }
+            if (n2 == 2) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t) mrow[t] -= XS[3 * 256 + i * 16 + t];
+            }
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc16(x, mrow, TS + (16 * b) * LDA + 16 * b + 4 * jq, LDA);
+            *reinterpret_cast<float4 *>(TS + (16 * a2 + i) * LDA + 16 * b + 4 * jq) = x;
+        }
+    }
+    __syncthreads();
     // T diag(b) as the K-major [64][64] A image, 16-byte stores (upper part zero)
     for (int e = tid; e < C * 8; e += PREP_THREADS) {
         const int rr = e >> 3, j8 = (e & 7) * 8;
@@ -438,21 +494,24 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (F) W rows -> record WQ rows 0..63 (warps 0-1); Ut -> record fp32 (warps 4-5)
+    // ---- (F) W rows -> record WQ rows 0..63 (warps 0-1); Ut -> record fp32 (warps 4-5);
+    //          two 16-column TMEM loads in flight per wait
     if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
         const int quarter = warp & 3;
         const int rr = 32 * quarter + lane;
         const bool isW = warp < 4;
+        const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16) + (isW ? 0 : 128);
         for (int cb = 0; cb < 4; ++cb) {
-            float val[32];
-            tmem_ld32(tmem + ((uint32_t)(32 * quarter) << 16) + (isW ? 0 : 128) + 32 * cb, val);
+            float lo[16], hi[16];
+            tmem_ld16(src + 32 * cb, lo);
+            tmem_ld16(src + 32 * cb + 16, hi);
             tmem_ld_wait();
             if (isW) {
 #pragma unroll
                 for (int i8 = 0; i8 < 4; ++i8) {
                     float x[8];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) x[i] = val[8 * i8 + i];
+                    for (int i = 0; i < 8; ++i) x[i] = i8 < 2 ? lo[8 * i8 + i] : hi[8 * (i8 - 2) + i];
                     *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(rr, 32 * cb + 8 * i8, 128)) = pack8(x);
                 }
             } else {
@@ -460,8 +519,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                 // chain kernel's row-per-thread reads hit distinct banks
                 float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + ((cb * 64 + rr) * 32) * 4);
 #pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4)
-                    dst[i4 ^ (rr & 7)] = make_float4(val[4 * i4], val[4 * i4 + 1], val[4 * i4 + 2], val[4 * i4 + 3]);
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float *v4 = i4 < 4 ? lo + 4 * i4 : hi + 4 * (i4 - 4);
+                    dst[i4 ^ (rr & 7)] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+                }
             }
         }
     }

@@ -41,10 +41,16 @@ inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline bool head_ok(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
 // Chunk length of the tensor-core path and the byte budget of one window of
-// chunk records: a window is produced by the prep kernel and consumed by the
-// chain kernel right after, so it is sized to stay resident in the 129 MB L2.
+// chunk records.  A window is produced by the prep kernel and consumed by the
+// chain kernel right after.  With few sequences the chain's parallelism is
+// (sequences in the window) x heads x column blocks whatever the window size,
+// so the window is kept small enough to stay resident in the 129 MB L2.  With
+// many sequences a large window lets the chain walk many sequences at once,
+// which matters more than L2 residency.
 constexpr int kTcChunk = 64;
-constexpr size_t kTcWindowBudget = 80u << 20;
+constexpr size_t kTcWindowBudgetFew = 80u << 20;
+constexpr size_t kTcWindowBudgetMany = 1u << 30;
+constexpr int32_t kManySeqs = 8;
 
 bool use_tc(int32_t dtype, int32_t dk, int32_t dv) {
     return dtype == KDA_BF16 && dk == 128 && dv == 128;
@@ -70,7 +76,8 @@ ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv
         L.rec_off = L.state_off + L.state_bytes;
         L.slots = chunk_slots(T, N, kTcChunk);
         const size_t rec = tc_record_bytes() * (size_t)H;
-        int64_t w = (int64_t)(kTcWindowBudget / rec);
+        const size_t budget = N >= kManySeqs ? kTcWindowBudgetMany : kTcWindowBudgetFew;
+        int64_t w = (int64_t)(budget / rec);
         if (w < 1) w = 1;
         L.window = L.slots < w ? L.slots : w;
         L.rec_bytes = (size_t)L.window * rec;

@@ -131,7 +131,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
-            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st) {
+            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st, int ahead) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -170,6 +170,23 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const uint4 zero = make_uint4(0, 0, 0, 0);
         kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
         qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
+    }
+    // The CTA `ahead` blocks later in launch order starts about one wave after this one:
+    // pull its q, k, z, v rows into L2 now (thread = (tensor, row), two 128-byte lines).
+    {
+        const int64_t lin = (int64_t)blockIdx.y * gridDim.x + blockIdx.x + ahead;
+        int n2 = 0, L2 = 0;
+        int64_t t2 = 0;
+        if (lin < (int64_t)gridDim.x * gridDim.y &&
+            slot_chunk(cu, chunk_off, N, slot0 + (int32_t)(lin % gridDim.x), n2, t2, L2)) {
+            const int tsel = tid >> 6, rr = tid & 63;
+            const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
+            if (rr < L2) {
+                const __nv_bfloat16 *row = src + ((t2 + rr) * H + (int)(lin / gridDim.x)) * (int64_t)DK;
+                prefetch_l2(row);
+                prefetch_l2(row + 64);
+            }
+        }
     }
     if (tid == 0) {
         mbar_init(&bar[0], 1);
@@ -541,7 +558,7 @@ constexpr uint32_t B_WQ = 0, B_KT = 32768, B_ZP = 49152, B_U = 65536, B_G = 7372
 constexpr uint32_t BUF_BYTES = 74752;
 constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
 constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
-constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, TMEM slot, abort flag
+constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, m3, TMEM slot, abort flag
 constexpr uint32_t C_SMEM = C_BAR + 64 + 1024;
 constexpr uint32_t LOAD_BYTES = 32768 + 16384 + 8192 + 8192 + 512;
 static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0, "chain buffer layout");
@@ -601,11 +618,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const int items = (n_last - n_first + 1) * H * NBLK;
     if ((int)blockIdx.x >= items) return;
 
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 32);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 40);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 40);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 48);
     if (tid == 0) {
-        for (int x = 0; x < 4; ++x) mbar_init(&bar[x], 1);
+        for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -656,8 +673,12 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                        records + ((size_t)(c_begin - slot0) * H + h) * REC_BYTES, blk,
                        &bar[gi & 1]);
 
-        // output rows of the chunk whose D1 buffer is `pb` (warps 2-3)
-        auto store_o = [&](int32_t cprev, uint32_t pb) {
+        // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
+        // (warps 2-3); waits for that chunk's [0; P] U product (barrier m3)
+        auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
+            const uint32_t pb = gprev & 1;
+            if (!mbar_wait(&bar[4], gprev & 1)) return false;
+            tc_fence_after();
             const int r = tid - 64;
             const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
             float oacc[32];
@@ -673,6 +694,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     dst[i8] = pack8(y);
                 }
             }
+            return true;
         };
 
         for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
@@ -690,11 +712,15 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     umma_bf16(tmem + 32 * b, ad, bd, id_km, s > 0);
                 }
                 umma_commit(&bar[2]);
-                // prefetch the next chunk into the other buffer (its last reader finished)
-                if (cs + 1 < c_end)
-                    chain_load(sm + (b ^ 1) * BUF_BYTES,
-                               records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
-                               &bar[b ^ 1]);
+                // prefetch the next chunk into the other buffer once its last reader, the
+                // previous chunk's [0; P] U product, has finished
+                if (cs + 1 < c_end) {
+                    if (cs > c_begin) ok = mbar_wait(&bar[4], (gi - 1) & 1);
+                    if (ok)
+                        chain_load(sm + (b ^ 1) * BUF_BYTES,
+                                   records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
+                                   &bar[b ^ 1]);
+                }
             }
             if (warp < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
@@ -717,7 +743,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     store_row_sw64(sm + C_UI, r, acc);
                 }
             } else if (cs > c_begin) {
-                store_o(cs - 1, b ^ 1);   // previous chunk's outputs, off the critical path
+                ok = store_o(cs - 1, gi - 1) && ok;   // previous chunk's outputs, off the critical path
             }
             if (!ok) *abort_flag = 1;
             fence_proxy_async();
@@ -726,15 +752,20 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             if (*abort_flag) break;
             if (tid == 0) {
                 tc_fence_after();
+                // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
                 for (int s = 0; s < C / 16; ++s) {
-                    // D2 = (K*Gam_C/Gam)^T U ;  D1[b] += [0; P] U
                     const uint64_t bd = sdesc_sw64(base + C_UI + s * 1024, 64 * 64, 512);
                     const uint64_t akt = sdesc_sw128(bufa + B_KT + s * 2048, 64 * 128, 1024);
                     umma_bf16(D2, akt, bd, id_mm, s > 0);
+                }
+                umma_commit(&bar[3]);
+                // ... then D1[b] += [0; P] U (outputs only), which runs while S is updated
+                for (int s = 0; s < C / 16; ++s) {
+                    const uint64_t bd = sdesc_sw64(base + C_UI + s * 1024, 64 * 64, 512);
                     const uint64_t azp = sdesc_sw128(bufa + B_ZP + s * 32, 16, 1024);
                     umma_bf16(tmem + 32 * b, azp, bd, id_km, 1);
                 }
-                umma_commit(&bar[3]);
+                umma_commit(&bar[4]);
             }
             ok = mbar_wait(&bar[3], gi & 1);
             tc_fence_after();
@@ -759,7 +790,9 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             if (tid == 0) report(st, KDA_ERR_TIMEOUT, ((int64_t)n * H + h) * NBLK + blk, 11);
         } else {
             tc_fence_after();
-            if (warp >= 2) store_o(c_end - 1, (gi - 1) & 1);   // the item's last chunk
+            bool ok_o = true;
+            if (warp >= 2) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (!ok_o) *abort_flag = 1;
 #pragma unroll
             for (int j4 = 0; j4 < DVB / 4; ++j4)
                 reinterpret_cast<float4 *>(srow)[j4] =
@@ -817,7 +850,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, s>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, records, st);
+            (int32_t)s0, records, st, 2 * sm_count);
         if (rec) rec->mark();
         // items of a window: at most min(N, window) sequences x H x NBLK
         const int64_t items = std::min<int64_t>(N, s1 - s0) * H * NBLK;

@@ -34,7 +34,8 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 
     __shared__ float s_k[DK], s_q[DK], s_alpha[DK];
     __shared__ float s_v[DV], s_u[DV];
-    __shared__ float s_pa[RPP][DV + 1], s_pb[RPP][DV + 1];
+    __shared__ __align__(16) float s_pa[RPP][DV];
+    __shared__ __align__(16) float s_pb[RPP][DV];
     __shared__ float s_qk, s_beta;
 
     const int nh = blockIdx.x;
@@ -82,11 +83,9 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         pa[0] += kr * s[p].x; pa[1] += kr * s[p].y; pa[2] += kr * s[p].z; pa[3] += kr * s[p].w;
         pb[0] += qr * s[p].x; pb[1] += qr * s[p].y; pb[2] += qr * s[p].z; pb[3] += qr * s[p].w;
     }
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        s_pa[rg][c4 * 4 + c] = pa[c];
-        s_pb[rg][c4 * 4 + c] = pb[c];
-    }
+    // one 16-byte store per thread: consecutive threads fill consecutive columns
+    *reinterpret_cast<float4 *>(&s_pa[rg][c4 * 4]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
+    *reinterpret_cast<float4 *>(&s_pb[rg][c4 * 4]) = make_float4(pb[0], pb[1], pb[2], pb[3]);
     __syncthreads();
     for (int j = tid; j < DV; j += kDecodeThreads) {
         float a = 0.f, b = 0.f;

@@ -71,6 +71,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
     }
 }
 
+// bring one line of global memory into L2 (no register result)
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 // ---------------------------------------------------------------- bulk TMA (1-D)
 // global -> shared, completion counted on `bar` (bytes and addresses: multiples of 16)
 __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,

@@ -55,7 +55,7 @@ constexpr uint32_t REC_G = 90112;
 constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
-constexpr int PREP_THREADS = 256;
+constexpr int PREP_THREADS = 512;
 constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and T tiles
 // Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
 // CTAs fit on one SM.  Regions are reused once the A/P products have completed.
@@ -121,10 +121,10 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
     return L > 0;
 }
 
-// One CTA per (chunk slot, head).  Work split for the element-wise passes:
-// warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2; lane l
-// takes row 16a + (l & 15); its four units are 8-channel chunks
-// ch = 8 (w >> 2) + 2u + (l >> 4), u = 0..3.  Scans over the 16 rows of a tile
+// One CTA per (chunk slot, head), 16 warps.  Work split for the element-wise
+// passes: warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2;
+// lane l takes row 16a + (l & 15); its two units are 8-channel chunks
+// ch = 4 (w >> 2) + 2u + (l >> 4), u = 0..1.  Scans over the 16 rows of a tile
 // run across the 16 lanes of a half-warp.
 __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
@@ -157,16 +157,16 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     const bool valid = r < L;
     const int64_t row_off = ((t0 + r) * H + h) * (int64_t)DK;
     // All of this thread's z, k and q chunks are requested before any set-up.
-    uint4 zraw[4], kraw[4], qraw[4];
+    uint4 zraw[2], kraw[2], qraw[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < 2; ++u) {
+        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
         const uint4 zero = make_uint4(0, 0, 0, 0);
         zraw[u] = valid ? *reinterpret_cast<const uint4 *>(z + row_off + c) : zero;
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < 2; ++u) {
+        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
         const uint4 zero = make_uint4(0, 0, 0, 0);
         kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
         qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
@@ -179,9 +179,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         int64_t t2 = 0;
         if (lin < (int64_t)gridDim.x * gridDim.y &&
             slot_chunk(cu, chunk_off, N, slot0 + (int32_t)(lin % gridDim.x), n2, t2, L2)) {
-            const int tsel = tid >> 6, rr = tid & 63;
+            const int tsel = (tid >> 6) & 3, rr = tid & 63;
             const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
-            if (rr < L2) {
+            if (tid < 256 && rr < L2) {
                 const __nv_bfloat16 *row = src + ((t2 + rr) * H + (int)(lin / gridDim.x)) * (int64_t)DK;
                 prefetch_l2(row);
                 prefetch_l2(row + 64);
@@ -202,10 +202,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
 
     // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check
-    float trun[4][8];
+    float trun[2][8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+    for (int u = 0; u < 2; ++u) {
+        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
         float zz[8];
         unpack8(zraw[u], zz);
 #pragma unroll
@@ -252,10 +252,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr] (smem), column-scaled K
     //          images (smem), Q*Gam and K*Gam_C/Gam (straight into the record)
-    uint4 kgam[4];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
+    uint4 kgam[2];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+    for (int u = 0; u < 2; ++u) {
+        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
         const int c = 8 * ch;
         float kk[8], qq[8], er[8], ktf[8];
         unpack8(kraw[u], kk);
@@ -318,10 +318,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         umma_commit(&bar[0]);
     }
     // prefetch this thread's V chunks while the products run
-    uint4 vv[4];
+    uint4 vv[2];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int ch = 8 * (warp >> 2) + 2 * u + (lane >> 4);
+    for (int u = 0; u < 2; ++u) {
+        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
         vv[u] = valid ? *reinterpret_cast<const uint4 *>(v + ((t0 + r) * H + h) * (int64_t)DV + 8 * ch)
                       : make_uint4(0, 0, 0, 0);
     }
@@ -330,8 +330,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        const int c = 8 * (8 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < 2; ++u) {
+        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = kgam[u];
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c, 64)) = vv[u];
     }
@@ -410,9 +410,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     };
     // N_ab = T_aa A_ab, in place over A (all reads happen before the barrier)
     {
-        float4 nv[2];
+        float4 nv[1];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
+        for (int w = 0; w < 1; ++w) {
             const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
             nv[w] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (task < 384) {
@@ -423,7 +423,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         __syncthreads();
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
+        for (int w = 0; w < 1; ++w) {
             const int task = tid + w * PREP_THREADS;
             if (task < 384) {
                 const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
@@ -458,7 +458,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     __syncthreads();
     // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise)
 #pragma unroll
-    for (int w = 0; w < 2; ++w) {
+    for (int w = 0; w < 1; ++w) {
         const int task = tid + w * PREP_THREADS;
         if (task < 384) {
             const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
@@ -513,12 +513,13 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (F) W rows -> record WQ rows 0..63 (warps 0-1); Ut -> record fp32 (warps 4-5);
     //          two 16-column TMEM loads in flight per wait
-    if (warp == 0 || warp == 1 || warp == 4 || warp == 5) {
+    if ((warp & 3) < 2) {   // warps 0,1,4,5 (W) and 8,9,12,13 (Ut); two column blocks each
         const int quarter = warp & 3;
         const int rr = 32 * quarter + lane;
-        const bool isW = warp < 4;
+        const bool isW = warp < 8;
+        const int cb0 = ((warp >> 2) & 1) * 2;
         const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16) + (isW ? 0 : 128);
-        for (int cb = 0; cb < 4; ++cb) {
+        for (int cb = cb0; cb < cb0 + 2; ++cb) {
             float lo[16], hi[16];
             tmem_ld16(src + 32 * cb, lo);
             tmem_ld16(src + 32 * cb + 16, hi);

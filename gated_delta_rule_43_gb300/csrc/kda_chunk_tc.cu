@@ -56,6 +56,11 @@ constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
 constexpr int PREP_THREADS = 512;
+constexpr int PREP_WARPS = PREP_THREADS / 32;
+constexpr int NU = 32 / PREP_WARPS;     // 8-channel units per thread in the element-wise passes
+constexpr int CHG = 2 * NU;             // 8-channel chunks per warp (per half-warp: NU)
+constexpr int SOLVE_W = (384 + PREP_THREADS - 1) / PREP_THREADS;   // solve tasks per thread
+static_assert(PREP_WARPS == 8 || PREP_WARPS == 16, "prep kernel runs 8 or 16 warps");
 constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and T tiles
 // Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
 // CTAs fit on one SM.  Regions are reused once the A/P products have completed.
@@ -67,7 +72,10 @@ constexpr uint32_t P_RT = 7680;         // fp32 [6][128]  exp(ref_a' - ref_a), a
 constexpr uint32_t P_KTF = 10752;       // fp32 [4][128]  exp(G_C - ref_a)
 constexpr uint32_t P_BETA = 12800;      // fp32 [64]
 constexpr uint32_t P_KRQR = 13312;      // K-major [128][128] row-scaled K/Q: tile a -> rows 32a..32a+31
-constexpr uint32_t P_KC = 46080;        // column-scaled K images, a = 0..3: [16(a+1)][128]
+constexpr uint32_t P_G = 13312;         // (before pass B) fp32 G scratch [64][GLD]
+constexpr int GLD = 132;                //   padded row stride: conflict-free row and column access
+constexpr uint32_t P_KC = 46080;        // column-scaled K images, a = 0..3, stacked: [160][128]
+constexpr uint32_t KC_ROWS = 160;       //   image a = rows 8a(a+1) .. 8a(a+1) + 16(a+1) - 1
 constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64][256]: K*Gam | V
 constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
@@ -78,6 +86,7 @@ constexpr uint32_t P_SMEM = P_END + 1024;
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
 static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
+static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
@@ -121,11 +130,11 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
     return L > 0;
 }
 
-// One CTA per (chunk slot, head), 16 warps.  Work split for the element-wise
-// passes: warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2;
-// lane l takes row 16a + (l & 15); its two units are 8-channel chunks
-// ch = 4 (w >> 2) + 2u + (l >> 4), u = 0..1.  Scans over the 16 rows of a tile
-// run across the 16 lanes of a half-warp.
+// One CTA per (chunk slot, head).  Work split for the row-wise element passes:
+// warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2; lane l
+// takes row 16a + (l & 15); its NU units are 8-channel chunks
+// ch = CHG (w >> 2) + 2u + (l >> 4), u = 0..NU-1.  The in-tile cumulative sums
+// run down the columns of a shared-memory scratch, one (tile, channel) per thread.
 __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
@@ -156,17 +165,19 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     const int r = 16 * a + rl;                 // this thread's row of the chunk
     const bool valid = r < L;
     const int64_t row_off = ((t0 + r) * H + h) * (int64_t)DK;
-    // All of this thread's z, k and q chunks are requested before any set-up.
-    uint4 zraw[2], kraw[2], qraw[2];
+    // All of this thread's global reads (A_log, beta, z, k, q) are issued before any set-up.
+    const float alog = A_log[h];
+    const float beta_v = tid < L ? __bfloat162float(beta[(t0 + min(tid, C - 1)) * H + h]) : 0.f;
+    uint4 zraw[NU], kraw[NU], qraw[NU];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
         const uint4 zero = make_uint4(0, 0, 0, 0);
         zraw[u] = valid ? *reinterpret_cast<const uint4 *>(z + row_off + c) : zero;
     }
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
         const uint4 zero = make_uint4(0, 0, 0, 0);
         kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
         qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
@@ -188,45 +199,57 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             }
         }
     }
+    const float expA = expf(alog);
+    if (tid < C) BETA[tid] = beta_v;
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         fence_mbar_init();
     }
-    if (warp == 0) {
+
+    // ---- (A) gate into the fp32 G scratch (row-wise, 16-byte stores), then the in-tile
+    //          inclusive cumsums down the columns: thread (tile, channel) walks its 16 rows,
+    //          leaves G in place, records the tile sum and checks the range
+    float *GS = reinterpret_cast<float *>(sm + P_G);
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
+        float zz[8];
+        unpack8(zraw[u], zz);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)   // g = -5 Sigmoid(e^A z), fast exponential and divide
+            zz[i] = valid ? __fdividef(kGMin, 1.0f + __expf(-expA * zz[i])) : 0.f;
+        float4 *dst = reinterpret_cast<float4 *>(GS + r * GLD + c);
+        dst[0] = make_float4(zz[0], zz[1], zz[2], zz[3]);
+        dst[1] = make_float4(zz[4], zz[5], zz[6], zz[7]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int e = tid; e < 4 * DK; e += PREP_THREADS) {
+        const int ta = e >> 7, c = e & (DK - 1);
+        float *col = GS + (16 * ta) * GLD + c;
+        float run = 0.f;
+        int bad_row = -1;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            run += col[i * GLD];
+            col[i * GLD] = run;
+            bad_row = (bad_row < 0 && 16 * ta + i < L && !decay_ok(run)) ? 16 * ta + i : bad_row;
+        }
+        TOT[ta * DK + c] = run;
+        if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
+    }
+    __syncthreads();
+    // this thread's G values, read before pass B reuses the scratch
+    float trun[NU][8];
+#pragma unroll
+    for (int u = 0; u < NU; ++u)
+        ld8(GS + r * GLD + 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4)), trun[u]);
+    if (warp == PREP_THREADS / 32 - 1) {   // idle during the table pass
         tmem_alloc(tslot, 256);
         tmem_relinquish();
         tc_fence_before();
     }
-    const float expA = expf(A_log[h]);
-    if (tid < C) BETA[tid] = tid < L ? __bfloat162float(beta[(t0 + tid) * H + h]) : 0.f;
-
-    // ---- (A) gate and in-tile inclusive cumsum (half-warp scans), tile sums, range check
-    float trun[2][8];
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
-        float zz[8];
-        unpack8(zraw[u], zz);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            // g = -5 Sigmoid(e^A z) with the fast exponential and divide (bf16 path)
-            float x = valid ? __fdividef(kGMin, 1.0f + __expf(-expA * zz[i])) : 0.f;
-#pragma unroll
-            for (int off = 1; off < 16; off <<= 1) {
-                const float y = __shfl_up_sync(0xffffffffu, x, off, 16);
-                if (rl >= off) x += y;
-            }
-            trun[u][i] = x;
-            if (valid && !decay_ok(x)) report(st, KDA_ERR_DECAY_RANGE, (t0 + r) * H + h, 5);
-        }
-        if (rl == 15) {
-            float4 *dst = reinterpret_cast<float4 *>(TOT + a * DK + 8 * ch);
-            dst[0] = make_float4(trun[u][0], trun[u][1], trun[u][2], trun[u][3]);
-            dst[1] = make_float4(trun[u][4], trun[u][5], trun[u][6], trun[u][7]);
-        }
-    }
-    __syncthreads();
     // tile references, Gam_C and the per-(tile, channel) factor tables
     if (tid < DK) {
         const int c = tid;
@@ -252,10 +275,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr] (smem), column-scaled K
     //          images (smem), Q*Gam and K*Gam_C/Gam (straight into the record)
-    uint4 kgam[2];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
+    uint4 kgam[NU];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
+    for (int u = 0; u < NU; ++u) {
+        const int ch = CHG * (warp >> 2) + 2 * u + (lane >> 4);
         const int c = 8 * ch;
         float kk[8], qq[8], er[8], ktf[8];
         unpack8(kraw[u], kk);
@@ -281,17 +304,16 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
         *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(64 + r, c, 128)) = pack8(qg);
         *reinterpret_cast<uint4 *>(rec + REC_KT + sw128_offset(r, c, 64)) = pack8(kt);
-        // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a)
-        uint32_t img = P_KC + 2048 * a * (a + 1);   // start of image a
-        *reinterpret_cast<uint4 *>(sm + img + sw128_offset(r, c, 16 * (a + 1))) = pack8(kf);
+        // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a);
+        // image a2 occupies rows 8 a2 (a2 + 1) .. of the stacked [160][128] B operand
+        *reinterpret_cast<uint4 *>(sm + P_KC + sw128_offset(8 * a * (a + 1) + r, c, KC_ROWS)) = pack8(kf);
 #pragma unroll
         for (int a2 = a + 1; a2 < 4; ++a2) {
-            img = P_KC + 2048 * a2 * (a2 + 1);
             float rt[8], x[8];
             ld8(RT + ((a2 * (a2 - 1)) / 2 + a) * DK + c, rt);
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = kf[i] * rt[i];
-            *reinterpret_cast<uint4 *>(sm + img + sw128_offset(r, c, 16 * (a2 + 1))) = pack8(x);
+            *reinterpret_cast<uint4 *>(sm + P_KC + sw128_offset(8 * a2 * (a2 + 1) + r, c, KC_ROWS)) = pack8(x);
         }
     }
     fence_proxy_async();
@@ -300,28 +322,23 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     const uint32_t tmem = *tslot;
     const uint32_t base = smem_u32(sm);
 
-    // ---- A and P: for each tile a, D_a = [Kr; Qr] x Kc_a^T (M = 128, N = 16(a+1), K = dk)
+    // ---- A and P: D = [Kr; Qr] x [Kc_0; Kc_1; Kc_2; Kc_3]^T (M = 128, N = 160, K = dk);
+    //      tile a's block D_a = [Kr; Qr] x Kc_a^T sits in columns 8 a (a + 1) .. + 16 (a + 1)
     if (tid == 0) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int rows = 16 * (t + 1);
-            const uint32_t idesc = idesc_bf16(128, rows, false, false);
-            const uint32_t img = base + P_KC + 2048 * t * (t + 1);
-            const uint32_t dcol = 8 * t * (t + 1);
-            for (int s = 0; s < DK / 16; ++s) {
-                const uint32_t koff = ((s * 16) % 64) * 2;
-                const uint64_t ad = sdesc_sw128(base + P_KRQR + (s >> 2) * 16384 + koff, 16, 1024);
-                const uint64_t bd = sdesc_sw128(img + (s >> 2) * rows * 128 + koff, 16, 1024);
-                umma_bf16(tmem + dcol, ad, bd, idesc, s > 0);
-            }
+        const uint32_t idesc = idesc_bf16(128, KC_ROWS, false, false);
+        for (int s = 0; s < DK / 16; ++s) {
+            const uint32_t koff = ((s * 16) % 64) * 2;
+            const uint64_t ad = sdesc_sw128(base + P_KRQR + (s >> 2) * 16384 + koff, 16, 1024);
+            const uint64_t bd = sdesc_sw128(base + P_KC + (s >> 2) * KC_ROWS * 128 + koff, 16, 1024);
+            umma_bf16(tmem, ad, bd, idesc, s > 0);
         }
         umma_commit(&bar[0]);
     }
     // prefetch this thread's V chunks while the products run
-    uint4 vv[2];
+    uint4 vv[NU];
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int ch = 4 * (warp >> 2) + 2 * u + (lane >> 4);
+    for (int u = 0; u < NU; ++u) {
+        const int ch = CHG * (warp >> 2) + 2 * u + (lane >> 4);
         vv[u] = valid ? *reinterpret_cast<const uint4 *>(v + ((t0 + r) * H + h) * (int64_t)DV + 8 * ch)
                       : make_uint4(0, 0, 0, 0);
     }
@@ -330,35 +347,44 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-        const int c = 8 * (4 * (warp >> 2) + 2 * u + (lane >> 4));
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = kgam[u];
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c, 64)) = vv[u];
     }
     // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
-    // warp t reads its own lane quarter, rows 32t.. of D_t
+    // warp w reads its own lane quarter t = w & 3 (rows 32t.. of D_t: 16 Kr rows, then
+    // 16 Qr rows), column blocks m = 2 (w >> 2) and 2 (w >> 2) + 1 of D_t
     float *AS = reinterpret_cast<float *>(sm + P_AS);
     float *TS = reinterpret_cast<float *>(sm + P_TS);
-    if (warp < 4) {
-        const int t = warp;
+    if (warp < 8) {   // eight warps: lane quarter t, two of the four column blocks
+        const int t = warp & 3, m0 = 2 * (warp >> 2);
         const bool isA = lane < 16;
         const int rr = 16 * t + (lane & 15);
         const float br = BETA[rr];
-        const uint32_t dcol = 8 * t * (t + 1);
-        for (int m = 0; m < 4; ++m) {
-            float val[16];
-            if (m <= t) {
-                tmem_ld16(tmem + ((uint32_t)(32 * t) << 16) + dcol + 16 * m, val);
-                tmem_ld_wait();
-            } else {
+        const uint32_t src = tmem + ((uint32_t)(32 * t) << 16) + 8 * t * (t + 1) + 16 * m0;
+        float val[2][16];
+        if (m0 <= t) tmem_ld16(src, val[0]);
+        if (m0 + 1 <= t) tmem_ld16(src + 16, val[1]);
+        tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) val[i] = 0.f;
+        for (int mm = 0; mm < 2; ++mm) {
+            const int m = m0 + mm;
+            if (m > t) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) val[mm][i] = 0.f;
             }
             if (isA) {
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int j = 16 * m + i;
-                    AS[rr * LDA + j] = (j < rr) ? br * val[i] : 0.f;
+                for (int i4 = 0; i4 < 4; ++i4) {
+                    float x[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int j = 16 * m + 4 * i4 + i;
+                        x[i] = (j < rr) ? br * val[mm][4 * i4 + i] : 0.f;
+                    }
+                    *reinterpret_cast<float4 *>(AS + rr * LDA + 16 * m + 4 * i4) =
+                        make_float4(x[0], x[1], x[2], x[3]);
                 }
             } else {
 #pragma unroll
@@ -367,7 +393,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
                         const int j = 16 * m + 8 * half + i;
-                        x[i] = (j <= rr) ? val[8 * half + i] : 0.f;
+                        x[i] = (j <= rr) ? val[mm][8 * half + i] : 0.f;
                     }
                     *reinterpret_cast<uint4 *>(rec + REC_P + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
                 }
@@ -410,9 +436,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     };
     // N_ab = T_aa A_ab, in place over A (all reads happen before the barrier)
     {
-        float4 nv[1];
+        float4 nv[SOLVE_W];
 #pragma unroll
-        for (int w = 0; w < 1; ++w) {
+        for (int w = 0; w < SOLVE_W; ++w) {
             const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
             nv[w] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (task < 384) {
@@ -423,7 +449,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         __syncthreads();
 #pragma unroll
-        for (int w = 0; w < 1; ++w) {
+        for (int w = 0; w < SOLVE_W; ++w) {
             const int task = tid + w * PREP_THREADS;
             if (task < 384) {
                 const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
@@ -458,7 +484,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     __syncthreads();
     // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise)
 #pragma unroll
-    for (int w = 0; w < 1; ++w) {
+    for (int w = 0; w < SOLVE_W; ++w) {
         const int task = tid + w * PREP_THREADS;
         if (task < 384) {
             const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
@@ -511,18 +537,19 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (F) W rows -> record WQ rows 0..63 (warps 0-1); Ut -> record fp32 (warps 4-5);
-    //          two 16-column TMEM loads in flight per wait
-    if ((warp & 3) < 2) {   // warps 0,1,4,5 (W) and 8,9,12,13 (Ut); two column blocks each
+    // ---- (F) W rows -> record WQ rows 0..63; Ut -> record fp32.  Rows 0..63 live in lane
+    //          quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut) x
+    //          (32-column block), two 16-column TMEM loads in flight per wait
+    if ((warp & 3) < 2) {
         const int quarter = warp & 3;
         const int rr = 32 * quarter + lane;
-        const bool isW = warp < 8;
-        const int cb0 = ((warp >> 2) & 1) * 2;
-        const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16) + (isW ? 0 : 128);
-        for (int cb = cb0; cb < cb0 + 2; ++cb) {
+        const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16);
+        for (int task = warp >> 2; task < 8; task += PREP_WARPS / 4) {
+            const bool isW = task < 4;
+            const int cb = task & 3;
             float lo[16], hi[16];
-            tmem_ld16(src + 32 * cb, lo);
-            tmem_ld16(src + 32 * cb + 16, hi);
+            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb, lo);
+            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb + 16, hi);
             tmem_ld_wait();
             if (isW) {
 #pragma unroll

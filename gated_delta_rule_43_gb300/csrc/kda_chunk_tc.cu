@@ -43,8 +43,6 @@ using namespace sm100;
 
 constexpr int C = 64;            // chunk length (four 16-token tiles)
 constexpr int DK = 128, DV = 128;
-constexpr int DVB = 32;          // value columns per chain CTA
-constexpr int NBLK = DV / DVB;
 
 // record layout (bytes)
 constexpr uint32_t REC_WQ = 0;
@@ -326,12 +324,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     //      tile a's block D_a = [Kr; Qr] x Kc_a^T sits in columns 8 a (a + 1) .. + 16 (a + 1)
     if (tid == 0) {
         const uint32_t idesc = idesc_bf16(128, KC_ROWS, false, false);
-        for (int s = 0; s < DK / 16; ++s) {
-            const uint32_t koff = ((s * 16) % 64) * 2;
-            const uint64_t ad = sdesc_sw128(base + P_KRQR + (s >> 2) * 16384 + koff, 16, 1024);
-            const uint64_t bd = sdesc_sw128(base + P_KC + (s >> 2) * KC_ROWS * 128 + koff, 16, 1024);
-            umma_bf16(tmem, ad, bd, idesc, s > 0);
-        }
+        const uint64_t ad = sdesc_sw128(base + P_KRQR, 16, 1024);
+        const uint64_t bd = sdesc_sw128(base + P_KC, 16, 1024);
+#pragma unroll
+        for (int s = 0; s < DK / 16; ++s)
+            umma_bf16(tmem, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                      desc_add(bd, (s >> 2) * KC_ROWS * 128 + (s & 3) * 32), idesc, s > 0);
         umma_commit(&bar[0]);
     }
     // prefetch this thread's V chunks while the products run
@@ -527,11 +525,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (tid == 0) {
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 256, false, true);
-        for (int s = 0; s < C / 16; ++s) {
-            const uint64_t ad = sdesc_sw128(base + P_TB + s * 32, 16, 1024);
-            const uint64_t bd = sdesc_sw128(base + P_KGV + s * 2048, 64 * 128, 1024);
-            umma_bf16(tmem, ad, bd, idesc, s > 0);
-        }
+        const uint64_t ad = sdesc_sw128(base + P_TB, 16, 1024);
+        const uint64_t bd = sdesc_sw128(base + P_KGV, 64 * 128, 1024);
+#pragma unroll
+        for (int s = 0; s < C / 16; ++s)
+            umma_bf16(tmem, desc_add(ad, s * 32), desc_add(bd, s * 2048), idesc, s > 0);
         umma_commit(&bar[1]);
     }
     ok = mbar_wait(&bar[1], 0) && ok;
@@ -580,7 +578,25 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     }
 }
 
-// ---------------------------------------------------------------- chain kernel
+// ---------------------------------------------------------------- chain kernels
+// largest n in [0, N) with chunk_off[n] <= slot (the owner of a used slot)
+__device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32_t slot) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (chunk_off[mid] <= slot) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+// ------------------------------------------------ chain kernel, 32-column blocks
+// The latency-bound shape: one CTA per (sequence, head, 32-column block of dv).  The
+// N = 32 products finish sooner than N = 128 ones, so a lone long sequence walks its
+// chunks fastest with four narrow CTAs per head.
+namespace c32 {
+
+constexpr int DVB = 32;          // value columns per CTA
+constexpr int NBLK = DV / DVB;
 constexpr int CHAIN_THREADS = 128;
 constexpr uint32_t B_WQ = 0, B_KT = 32768, B_ZP = 49152, B_U = 65536, B_G = 73728;
 constexpr uint32_t BUF_BYTES = 74752;
@@ -601,16 +617,6 @@ __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int
     bulk_g2s(buf + B_ZP + 8192, rec + REC_P, 8192, full);
     bulk_g2s(buf + B_U, rec + REC_U + blk * 8192, 8192, full);
     bulk_g2s(buf + B_G, rec + REC_G, 512, full);
-}
-
-// largest n in [0, N) with chunk_off[n] <= slot (the owner of a used slot)
-__device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32_t slot) {
-    int lo = 0, hi = N - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (chunk_off[mid] <= slot) lo = mid; else hi = mid - 1;
-    }
-    return lo;
 }
 
 // 32 fp32 values -> four 16-byte chunks of row r of a 64B-swizzled MN-major image
@@ -672,6 +678,8 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const uint32_t base = smem_u32(sm);
     const uint32_t id_km = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
     const uint32_t id_mm = idesc_bf16(128, DVB, true, true);    // A MN-major, B MN-major
+    const uint64_t bd_s = sdesc_sw64(base + C_S, 128 * 64, 512);    // S image, K step 0
+    const uint64_t bd_u = sdesc_sw64(base + C_UI, 64 * 64, 512);    // U image, K step 0
     const int i = tid;  // this thread's state row
     uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
@@ -733,22 +741,12 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             if (tid == 0 && ok) {
                 // D1[b] = [W; Q*Gam] S
                 tc_fence_after();
-                for (int s = 0; s < DK / 16; ++s) {
-                    const uint32_t koff = ((s * 16) % 64) * 2;
-                    const uint64_t ad = sdesc_sw128(bufa + B_WQ + (s >> 2) * 16384 + koff, 16, 1024);
-                    const uint64_t bd = sdesc_sw64(base + C_S + s * 1024, 128 * 64, 512);
-                    umma_bf16(tmem + 32 * b, ad, bd, id_km, s > 0);
-                }
+                const uint64_t ad = sdesc_sw128(bufa + B_WQ, 16, 1024);
+#pragma unroll
+                for (int s = 0; s < DK / 16; ++s)
+                    umma_bf16(tmem + 32 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                              desc_add(bd_s, s * 1024), id_km, s > 0);
                 umma_commit(&bar[2]);
-                // prefetch the next chunk into the other buffer once its last reader, the
-                // previous chunk's [0; P] U product, has finished
-                if (cs + 1 < c_end) {
-                    if (cs > c_begin) ok = mbar_wait(&bar[4], (gi - 1) & 1);
-                    if (ok)
-                        chain_load(sm + (b ^ 1) * BUF_BYTES,
-                                   records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
-                                   &bar[b ^ 1]);
-                }
             }
             if (warp < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
@@ -770,8 +768,14 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     }
                     store_row_sw64(sm + C_UI, r, acc);
                 }
-            } else if (cs > c_begin) {
-                ok = store_o(cs - 1, gi - 1) && ok;   // previous chunk's outputs, off the critical path
+            } else {
+                // previous chunk's outputs, off the critical path; its [0; P] U product was
+                // the last reader of the other buffer, which then takes the next chunk
+                if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
+                if (tid == 64 && ok && cs + 1 < c_end)
+                    chain_load(sm + (b ^ 1) * BUF_BYTES,
+                               records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
+                               &bar[b ^ 1]);
             }
             if (!ok) *abort_flag = 1;
             fence_proxy_async();
@@ -781,18 +785,16 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             if (tid == 0) {
                 tc_fence_after();
                 // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
-                for (int s = 0; s < C / 16; ++s) {
-                    const uint64_t bd = sdesc_sw64(base + C_UI + s * 1024, 64 * 64, 512);
-                    const uint64_t akt = sdesc_sw128(bufa + B_KT + s * 2048, 64 * 128, 1024);
-                    umma_bf16(D2, akt, bd, id_mm, s > 0);
-                }
+                const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
+#pragma unroll
+                for (int s = 0; s < C / 16; ++s)
+                    umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
                 umma_commit(&bar[3]);
                 // ... then D1[b] += [0; P] U (outputs only), which runs while S is updated
-                for (int s = 0; s < C / 16; ++s) {
-                    const uint64_t bd = sdesc_sw64(base + C_UI + s * 1024, 64 * 64, 512);
-                    const uint64_t azp = sdesc_sw128(bufa + B_ZP + s * 32, 16, 1024);
-                    umma_bf16(tmem + 32 * b, azp, bd, id_km, 1);
-                }
+                const uint64_t azp = sdesc_sw128(bufa + B_ZP, 16, 1024);
+#pragma unroll
+                for (int s = 0; s < C / 16; ++s)
+                    umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024), id_km, 1);
                 umma_commit(&bar[4]);
             }
             ok = mbar_wait(&bar[3], gi & 1);
@@ -836,6 +838,256 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     }
 }
 
+}  // namespace c32
+
+// ----------------------------------------------- chain kernel, all 128 columns
+namespace c128 {
+
+// One CTA per work item (sequence, head) owns all dv = 128 columns of S: the
+// products below are M = 128, N = 128, which cost the tensor core about as much
+// per instruction as N = 32, so one CTA does the work four narrower ones would.
+constexpr int CHAIN_THREADS = 512;
+constexpr uint32_t C_S = 0;                          // S image, MN-major SW128 [128 k][128 n]
+constexpr uint32_t C_UI = 32768;                     // U image, MN-major SW128 [64 k][128 n]
+constexpr uint32_t C_BUF0 = 49152;                   // record buffer 0 (REC_BYTES)
+constexpr uint32_t C_BAR = C_BUF0 + REC_BYTES;       // full[2], m1, m2, m3, TMEM slot, abort flag
+constexpr uint32_t C_BUF1 = 140288;                  // record buffer 1
+constexpr uint32_t C_SMEM = C_BUF1 + REC_BYTES + 1024;
+static_assert(C_BAR + 64 <= C_BUF1 && C_BUF1 % 1024 == 0 && C_BUF0 % 1024 == 0,
+              "chain buffer layout");
+static_assert(REC_P % 1024 == 0 && REC_KT % 1024 == 0 && REC_U % 1024 == 0, "record alignment");
+static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
+
+__device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, uint64_t *full) {
+    mbar_arrive_expect_tx(full, REC_BYTES);
+    bulk_g2s(buf + REC_WQ, rec + REC_WQ, REC_KT - REC_WQ, full);
+    bulk_g2s(buf + REC_KT, rec + REC_KT, REC_P - REC_KT, full);
+    bulk_g2s(buf + REC_P, rec + REC_P, REC_U - REC_P, full);
+    bulk_g2s(buf + REC_U, rec + REC_U, REC_G - REC_U, full);
+    bulk_g2s(buf + REC_G, rec + REC_G, REC_BYTES - REC_G, full);
+}
+
+// 32 fp32 values -> four 16-byte chunks of row r, columns j0.., of a 128B-swizzled
+// MN-major image whose 64-column groups are `rows` * 128 bytes apart
+__device__ __forceinline__ void store_row_sw128(uint8_t *img, int r, int j0, uint32_t rows,
+                                                const float (&x)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = x[8 * c8 + i];
+        *reinterpret_cast<uint4 *>(img + sw128_offset(r, j0 + 8 * c8, rows)) = pack8(y);
+    }
+}
+
+// Persistent over work items (sequence, head) of the sequences that own chunks in
+// the slot window [slot0, slot1); each item walks its chunks in order.  Warp w
+// holds lane quarter q = w & 3 and column block cb = w >> 2: thread (row 32q +
+// lane, columns 32cb..32cb+31) keeps its piece of S in registers (fp32), and S is
+// mirrored as the bf16 B operand image.  Per chunk, on the critical path:
+//   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
+//   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
+// ([x; P] reads the 64 rows in front of P as its first half; those rows of D1
+// hold W S, which has been consumed by then.)  D1 is double-buffered in TMEM so
+// that the output rows of chunk c (D1[64:128], lane quarters 2-3) are stored while
+// lane quarters 0-1 form U of chunk c+1.
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
+             int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
+             float *__restrict__ state, __nv_bfloat16 *__restrict__ o, StatusWord *st) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t used = min(slot1, chunk_off[N]);
+    if (slot0 >= used) return;
+    const int n_first = slot_owner(chunk_off, N, slot0);
+    const int n_last = slot_owner(chunk_off, N, used - 1);
+    const int items = (n_last - n_first + 1) * H;
+    if ((int)blockIdx.x >= items) return;
+
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 40);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 48);
+    if (tid == 0) {
+        for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t D2 = tmem + 256;                    // D1 buffers at columns 0 and 128
+    const int q4 = warp & 3, cb = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const uint32_t base = smem_u32(sm);
+    const uint32_t id_km = idesc_bf16(128, DV, false, true);   // A K-major, B MN-major
+    const uint32_t id_mm = idesc_bf16(128, DV, true, true);    // A MN-major, B MN-major
+    const uint64_t bd_s = sdesc_sw128(base + C_S, DK * 128, 1024);   // S image, K step 0
+    const uint64_t bd_u = sdesc_sw128(base + C_UI, C * 128, 1024);   // U image, K step 0
+    const int i = 32 * q4 + lane;   // this thread's state row
+    const int j0 = 32 * cb;         // and first column
+    uint32_t gi = 0;                // chunks processed by this CTA (drives buffer and barrier parity)
+    auto buf_off = [](uint32_t b) { return b ? C_BUF1 : C_BUF0; };
+
+    for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
+        const int h = item % H;
+        const int n = n_first + item / H;
+        const int32_t cfirst = chunk_off[n];
+        const int32_t c_begin = max(cfirst, slot0);
+        const int32_t c_end = min(chunk_off[n + 1], slot1);
+        if (c_begin >= c_end) continue;
+        const int64_t bos = cu[n];
+        const int64_t eos = cu[n + 1];
+        float S[32];
+        float *srow = state + (((int64_t)n * H + h) * DK + i) * DV + j0;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
+            S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+        }
+        store_row_sw128(sm + C_S, i, j0, DK, S);
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 0)
+            chain_load(sm + buf_off(gi & 1),
+                       records + ((size_t)(c_begin - slot0) * H + h) * REC_BYTES, &bar[gi & 1]);
+
+        // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
+        // (lane quarters 2-3); waits for that chunk's [x; P] U product (barrier m3)
+        auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
+            const uint32_t pb = gprev & 1;
+            if (!mbar_wait(&bar[4], gprev & 1)) return false;
+            tc_fence_after();
+            const int r = i - 64;
+            const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
+            float oacc[32];
+            tmem_ld32(tmem + 128 * pb + lane_base + j0, oacc);
+            tmem_ld_wait();
+            if (t < eos) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8) {
+                    float y[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) y[x] = oacc[8 * i8 + x];
+                    dst[i8] = pack8(y);
+                }
+            }
+            return true;
+        };
+
+        for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
+            const uint32_t b = gi & 1;
+            uint8_t *buf = sm + buf_off(b);
+            const uint32_t bufa = base + buf_off(b);
+            bool ok = mbar_wait(&bar[b], (gi >> 1) & 1);
+            if (tid == 0 && ok) {
+                // D1[b] = [W; Q*Gam] S
+                tc_fence_after();
+                const uint64_t ad = sdesc_sw128(bufa + REC_WQ, 16, 1024);
+#pragma unroll
+                for (int s = 0; s < DK / 16; ++s)
+                    umma_bf16(tmem + 128 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                              desc_add(bd_s, s * 2048), id_km, s > 0);
+                umma_commit(&bar[2]);
+            }
+            if (q4 < 2) {
+                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
+                ok = ok && mbar_wait(&bar[2], gi & 1);
+                tc_fence_after();
+                if (ok) {
+                    const int r = i;
+                    float acc[32];
+                    tmem_ld32(tmem + 128 * b + lane_base + j0, acc);
+                    tmem_ld_wait();
+                    const float4 *ut = reinterpret_cast<const float4 *>(buf + REC_U + (cb * 64 + r) * 128);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 u4 = ut[j4 ^ (r & 7)];
+                        acc[4 * j4 + 0] = u4.x - acc[4 * j4 + 0];
+                        acc[4 * j4 + 1] = u4.y - acc[4 * j4 + 1];
+                        acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
+                        acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
+                    }
+                    store_row_sw128(sm + C_UI, r, j0, C, acc);
+                }
+            } else {
+                // previous chunk's outputs, off the critical path; its [x; P] U product was
+                // the last reader of the other buffer, which then takes the next chunk
+                if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
+                if (tid == 64 && ok && cs + 1 < c_end)
+                    chain_load(sm + buf_off(b ^ 1),
+                               records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES,
+                               &bar[b ^ 1]);
+            }
+            if (!ok) *abort_flag = 1;
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (*abort_flag) break;
+            if (tid == 0) {
+                tc_fence_after();
+                // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
+                const uint64_t akt = sdesc_sw128(bufa + REC_KT, C * 128, 1024);
+#pragma unroll
+                for (int s = 0; s < C / 16; ++s)
+                    umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 2048), id_mm, s > 0);
+                umma_commit(&bar[3]);
+                // ... then D1[b] += [x; P] U (outputs only), which runs while S is updated
+                const uint64_t azp = sdesc_sw128(bufa + REC_P - 8192, 16, 1024);
+#pragma unroll
+                for (int s = 0; s < C / 16; ++s)
+                    umma_bf16(tmem + 128 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 2048), id_km, 1);
+                umma_commit(&bar[4]);
+            }
+            ok = mbar_wait(&bar[3], gi & 1);
+            tc_fence_after();
+            if (ok) {
+                // S <- Diag(Gam_C) S + D2 (row i, columns j0..)
+                const float gc = reinterpret_cast<const float *>(buf + REC_G)[i];
+                float acc[32];
+                tmem_ld32(D2 + lane_base + j0, acc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + acc[j];
+                store_row_sw128(sm + C_S, i, j0, DK, S);
+            } else {
+                *abort_flag = 1;
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (*abort_flag) break;
+        }
+        if (*abort_flag) {
+            if (tid == 0) report(st, KDA_ERR_TIMEOUT, (int64_t)n * H + h, 11);
+        } else {
+            tc_fence_after();
+            bool ok_o = true;
+            if (q4 >= 2) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (!ok_o) *abort_flag = 1;
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4)
+                reinterpret_cast<float4 *>(srow)[j4] =
+                    make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace c128
+
 // Copy (or zero) the initial state into the running-state buffer.
 __global__ void state_init_kernel(const float *__restrict__ h0, float *__restrict__ S,
                                   int64_t n4) {
@@ -859,8 +1111,11 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C_SMEM);
+    e = cudaFuncSetAttribute(c32::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)c32::C_SMEM);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(c128::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)c128::C_SMEM);
     if (e != cudaSuccess) return e;
     int dev = 0, sm_count = 0;
     e = cudaGetDevice(&dev);
@@ -880,12 +1135,22 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
             (int32_t)s0, records, st, 2 * sm_count);
         if (rec) rec->mark();
-        // items of a window: at most min(N, window) sequences x H x NBLK
-        const int64_t items = std::min<int64_t>(N, s1 - s0) * H * NBLK;
-        const int64_t grid = std::min<int64_t>(items, sm_count);
-        chain_kernel<<<(unsigned)grid, CHAIN_THREADS, C_SMEM, s>>>(
-            cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, S_run, (__nv_bfloat16 *)o,
-            st);
+        // A window holds at most min(N, window) sequences.  While their 32-column items
+        // fit in about two waves the chain is latency-bound and the narrow kernel walks
+        // the chunks fastest; with more items the 128-column kernel, which does the same
+        // work in about half the SM time, finishes first.
+        const int64_t seqs = std::min<int64_t>(N, s1 - s0);
+        if (seqs * H * c32::NBLK <= 2 * (int64_t)sm_count) {
+            const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
+            c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, s>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, S_run,
+                (__nv_bfloat16 *)o, st);
+        } else {
+            const int64_t grid = std::min<int64_t>(seqs * H, sm_count);
+            c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, s>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, S_run,
+                (__nv_bfloat16 *)o, st);
+        }
         if (rec) rec->mark();
     }
     return cudaGetLastError();

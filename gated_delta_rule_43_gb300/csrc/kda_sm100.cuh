@@ -216,6 +216,12 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
         : "memory");
 }
 
+// A descriptor whose start address is `bytes` further on (the start-address field holds
+// addr >> 4 in 14 bits; shared-memory offsets stay below 256 KB, so there is no carry).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) {
+    return d + (uint64_t)(bytes >> 4);
+}
+
 // Byte offset of element (r, k) in a K-major 128B-swizzled image whose atom
 // columns (64 K each) hold `rows` rows; MN-major images use the same formula
 // with (r, k) = (k-row, mn-element) and `rows` = K extent.

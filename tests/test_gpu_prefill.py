@@ -94,3 +94,23 @@ def test_prefill_1m_workload_sampled():
     """B=1, H=16, T=1,048,576: full GPU run, two heads scored over the whole length."""
     d = inputs.make_workload(inputs.WORKLOADS["prefill_1m"], device=DEV)
     _run_and_score(d, "bf16", heads=[0, 15])
+
+
+def _chain_shape(N, H):
+    """Which chain kernel the library runs for N sequences of H heads (dk = dv = 128, bf16):
+    32-column items while N*H*4 fits in two waves of the device's SMs, else 128-column."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 32 if N * H * 4 <= 2 * sms else 128
+
+
+@pytest.mark.parametrize("lens", [[130, 257], [130, 257, 64, 3] * 3],
+                         ids=["few-seqs", "many-seqs"])
+def test_both_chain_shapes(lens):
+    """The narrow (32-column) and wide (128-column) chain kernels, with initial states and
+    ragged chunks; the two cases are chosen so that they select different kernels."""
+    H = 32
+    shapes = {_chain_shape(len(l), H) for l in [[130, 257], [130, 257, 64, 3] * 3]}
+    assert shapes == {32, 128}
+    d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=len(lens),
+                            h0_sigma=0.1, device=DEV)
+    _run_and_score(d, "bf16")

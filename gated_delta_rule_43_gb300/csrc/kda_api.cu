@@ -23,7 +23,8 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                             const void *beta, const float *A_log, const int32_t *cu,
                             const int32_t *chunk_off, int N, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
-                            int64_t window, StatusWord *st, cudaStream_t s, EventRec *rec);
+                            int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
+                            EventRec *rec);
 int64_t chunk_slots(int64_t T_tot, int N, int C);
 cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
                         const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
@@ -40,17 +41,15 @@ inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline bool aligned(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline bool head_ok(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
-// Chunk length of the tensor-core path and the byte budget of one window of
-// chunk records.  A window is produced by the prep kernel and consumed by the
-// chain kernel right after.  With few sequences the chain's parallelism is
-// (sequences in the window) x heads x column blocks whatever the window size,
-// so the window is kept small enough to stay resident in the 129 MB L2.  With
-// many sequences a large window lets the chain walk many sequences at once,
-// which matters more than L2 residency.
+// Chunk length of the tensor-core path and the byte budget of the chunk records.
+// A window of records is produced by the prep kernel and consumed by the chain
+// kernel.  Every window costs a ramp and a tail of both kernels, which measured
+// more than the DRAM round trip of the records, so windows are large: a problem
+// whose records fit the budget runs as one window; a larger one is cut into
+// windows of half the budget, double-buffered so that the prep of window w + 1
+// runs beside the chain of window w.
 constexpr int kTcChunk = 64;
-constexpr size_t kTcWindowBudgetFew = 80u << 20;
-constexpr size_t kTcWindowBudgetMany = 1u << 30;
-constexpr int32_t kManySeqs = 8;
+constexpr size_t kTcRecordBudget = 1u << 30;
 
 bool use_tc(int32_t dtype, int32_t dk, int32_t dv) {
     return dtype == KDA_BF16 && dk == 128 && dv == 128;
@@ -59,8 +58,9 @@ bool use_tc(int32_t dtype, int32_t dk, int32_t dv) {
 struct ChunkLayout {
     size_t plan_off, plan_bytes;
     size_t state_off, state_bytes;   // running state of the tensor-core path
-    size_t rec_off, rec_bytes;       // one window of chunk records
+    size_t rec_off, rec_bytes;       // one or two windows of chunk records
     int64_t slots, window;
+    int nbuf;                        // record buffers: 2 when there is more than one window
     size_t total;
 };
 
@@ -76,11 +76,16 @@ ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv
         L.rec_off = L.state_off + L.state_bytes;
         L.slots = chunk_slots(T, N, kTcChunk);
         const size_t rec = tc_record_bytes() * (size_t)H;
-        const size_t budget = N >= kManySeqs ? kTcWindowBudgetMany : kTcWindowBudgetFew;
-        int64_t w = (int64_t)(budget / rec);
+        int64_t w = (int64_t)(kTcRecordBudget / rec);
         if (w < 1) w = 1;
-        L.window = L.slots < w ? L.slots : w;
-        L.rec_bytes = (size_t)L.window * rec;
+        if (L.slots <= w) {
+            L.window = L.slots;
+            L.nbuf = 1;
+        } else {
+            L.window = w / 2 > 0 ? w / 2 : 1;
+            L.nbuf = 2;
+        }
+        L.rec_bytes = (size_t)L.nbuf * L.window * rec;
     }
     L.total = L.rec_off + L.rec_bytes;
     return L;
@@ -127,15 +132,15 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
         uint8_t *ws = (uint8_t *)workspace;
         int32_t *chunk_off = (int32_t *)(ws + L.plan_off);
         float *S_run = final_state ? final_state : (float *)(ws + L.state_off);
-        if (rec) rec->mark();
+        if (rec) rec->mark(s);
         e = launch_plan(cu_seqlens, num_seqs, total_tokens, kTcChunk, chunk_off, st, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
-        if (rec) rec->mark();
+        if (rec) rec->mark(s);
         e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs, L.slots, H,
-                            initial_state, S_run, o, ws + L.rec_off, L.window, st, s, rec);
+                            initial_state, S_run, o, ws + L.rec_off, L.window, L.nbuf, st, s,
+                            rec);
         return cuda_status(e);
     }
-    if (rec) rec->mark();
     e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
                           total_tokens, H, initial_state, final_state, o, st, s, rec);
     return cuda_status(e);
@@ -193,7 +198,6 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
     EventRec rec;
     rec.ev = (cudaEvent_t *)events;
     rec.cap = n_events;
-    rec.s = (cudaStream_t)stream;
     const kda_status r = chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
                                         total_tokens, H, dk, dv, dtype, initial_state,
                                         final_state, o, workspace, workspace_bytes, stream, &rec);

@@ -209,10 +209,11 @@ static cudaError_t launch_simt_t(const void *q, const void *k, const void *v, co
     if (e != cudaSuccess) return e;
     const int64_t grid = (int64_t)N * H * (dv / kSimtDVB);
     if (grid <= 0) return cudaSuccess;
+    if (rec) rec->mark(s);
     kern<<<(unsigned)grid, kSimtThreads, smem, s>>>((const T *)q, (const T *)k, (const T *)v,
                                                     (const T *)z, (const T *)beta, A_log, cu, N,
                                                     T_tot, H, dv, h0, hT, (T *)o, st);
-    if (rec) rec->mark();
+    if (rec) rec->mark(s);
     return cudaGetLastError();
 }
 

@@ -32,6 +32,7 @@
 //   Ut  fp32 [4 column blocks][64][32], float4 slot j4 of row r holds columns 4 (j4 ^ (r % 8))
 //   GC  fp32 [128] Gam_C
 #include <algorithm>
+#include <mutex>
 
 #include "kda_common.cuh"
 #include "kda_sm100.cuh"
@@ -1101,11 +1102,53 @@ __global__ void state_init_kernel(const float *__restrict__ h0, float *__restric
 
 size_t tc_record_bytes() { return tc::REC_BYTES; }
 
+namespace {
+
+// Streams and events of the double-buffered schedule, created once per device and
+// kept for the life of the process.  Two low-priority streams take the prep
+// kernels of even and odd windows, one high-priority stream the chain kernels; the
+// block scheduler then hands freed SMs to a waiting chain CTA first.
+struct Pipe {
+    bool ready = false;
+    cudaStream_t prep[2] = {nullptr, nullptr};
+    cudaStream_t chain = nullptr;
+    cudaEvent_t start = nullptr, end = nullptr;
+    cudaEvent_t prep_done[2] = {nullptr, nullptr}, chain_done[2] = {nullptr, nullptr};
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_pipe_mutex;     // held while a call enqueues its schedule
+Pipe g_pipe[kMaxDevices];
+
+cudaError_t pipe_setup(int dev, Pipe *&out) {
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    Pipe &P = g_pipe[dev];
+    out = &P;
+    if (P.ready) return cudaSuccess;
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+        e = cudaStreamCreateWithPriority(&P.prep[i], cudaStreamNonBlocking, least);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&P.chain, cudaStreamNonBlocking, greatest);
+    cudaEvent_t *evs[6] = {&P.start, &P.end, &P.prep_done[0], &P.prep_done[1],
+                           &P.chain_done[0], &P.chain_done[1]};
+    for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+        e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
+    if (e == cudaSuccess) P.ready = true;
+    return e;
+}
+
+}  // namespace
+
+// Records: nbuf (1 or 2) buffers of `window` chunk slots x H records each.  With one
+// buffer the windows run prep, chain, prep, chain ... on `s`.  With two, prep of
+// window w + 1 runs beside chain of window w (see Pipe); the call's work is still
+// ordered after everything enqueued on `s` before it and before everything after it.
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
                             const int32_t *chunk_off, int N, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
-                            int64_t window, StatusWord *st, cudaStream_t s, EventRec *rec) {
+                            int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
+                            EventRec *rec) {
     using namespace tc;
     cudaError_t e = cudaFuncSetAttribute(prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1124,34 +1167,77 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
     const int64_t n4 = (int64_t)N * H * DK * DV / 4;
     if (h0 != S_run) {
         const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count * 16);
+        if (rec) rec->mark(s);
         state_init_kernel<<<(unsigned)blocks, 256, 0, s>>>(h0, S_run, n4);
-        if (rec) rec->mark();
+        if (rec) rec->mark(s);
     }
-    for (int64_t s0 = 0; s0 < slots; s0 += window) {
+    const bool piped = nbuf == 2 && slots > window;
+    Pipe *P = nullptr;
+    std::unique_lock<std::mutex> lock(g_pipe_mutex, std::defer_lock);
+    if (piped) {
+        lock.lock();
+        e = pipe_setup(dev, P);
+        if (e != cudaSuccess) return e;
+        e = cudaEventRecord(P->start, s);
+        for (int i = 0; i < 2 && e == cudaSuccess; ++i) e = cudaStreamWaitEvent(P->prep[i], P->start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(P->chain, P->start, 0);
+        if (e != cudaSuccess) return e;
+    }
+    const size_t buf_bytes = (size_t)window * H * REC_BYTES;
+    int64_t w = 0;
+    for (int64_t s0 = 0; s0 < slots; s0 += window, ++w) {
         const int64_t s1 = std::min(slots, s0 + window);
+        const int par = (int)(w & 1);
+        uint8_t *recs = records + (piped ? par * buf_bytes : 0);
+        cudaStream_t sp = piped ? P->prep[par] : s;
+        cudaStream_t sc = piped ? P->chain : s;
+        // prep of window w; with two buffers, after the chain of window w - 2 has read
+        // this buffer
+        if (piped && w >= 2) {
+            e = cudaStreamWaitEvent(sp, P->chain_done[par], 0);
+            if (e != cudaSuccess) return e;
+        }
         dim3 pg((unsigned)(s1 - s0), (unsigned)H);
-        prep_kernel<<<pg, PREP_THREADS, P_SMEM, s>>>(
+        if (rec) rec->mark(sp);
+        prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, records, st, 2 * sm_count);
-        if (rec) rec->mark();
+            (int32_t)s0, recs, st, 2 * sm_count);
+        if (rec) rec->mark(sp);
+        if (piped) {
+            e = cudaEventRecord(P->prep_done[par], sp);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, P->prep_done[par], 0);
+            if (e != cudaSuccess) return e;
+        }
         // A window holds at most min(N, window) sequences.  While their 32-column items
         // fit in about two waves the chain is latency-bound and the narrow kernel walks
         // the chunks fastest; with more items the 128-column kernel, which does the same
-        // work in about half the SM time, finishes first.
+        // work in about half the SM time, finishes first.  Beside a prep kernel the
+        // narrow one is kept only while it leaves at least half of the SMs to the prep.
         const int64_t seqs = std::min<int64_t>(N, s1 - s0);
-        if (seqs * H * c32::NBLK <= 2 * (int64_t)sm_count) {
+        const int64_t items32 = seqs * H * c32::NBLK;
+        if (rec) rec->mark(sc);
+        if (items32 <= (piped ? (int64_t)sm_count / 2 : 2 * (int64_t)sm_count)) {
             const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
-            c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, s>>>(
-                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, S_run,
+            c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, sc>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, S_run,
                 (__nv_bfloat16 *)o, st);
         } else {
             const int64_t grid = std::min<int64_t>(seqs * H, sm_count);
-            c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, s>>>(
-                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, S_run,
+            c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, sc>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, S_run,
                 (__nv_bfloat16 *)o, st);
         }
-        if (rec) rec->mark();
+        if (rec) rec->mark(sc);
+        if (piped) {
+            e = cudaEventRecord(P->chain_done[par], sc);
+            if (e != cudaSuccess) return e;
+        }
+    }
+    if (piped) {
+        e = cudaEventRecord(P->end, P->chain);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P->end, 0);
+        if (e != cudaSuccess) return e;
     }
     return cudaGetLastError();
 }

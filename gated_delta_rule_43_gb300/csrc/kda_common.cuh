@@ -31,8 +31,8 @@ struct EventRec {
     cudaEvent_t *ev = nullptr;
     int cap = 0;
     int used = 0;
-    cudaStream_t s = nullptr;
-    void mark() {
+    // records the next event on `s`; each kernel is bracketed by two marks on its own stream
+    void mark(cudaStream_t s) {
         if (ev && used < cap) cudaEventRecord(ev[used++], s);
     }
 };

@@ -30,7 +30,8 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                             const void *beta, const float *A_log, const int32_t *cu,
                             const int32_t *chunk_off, int N, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
-                            int64_t window, StatusWord *st, cudaStream_t s, EventRec *rec);
+                            int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
+                            EventRec *rec);
 cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const void *k,
                               const void *v, const void *z, const void *beta,
                               const float *A_log, const int32_t *cu, int N, int64_t T_tot, int H,
@@ -131,8 +132,8 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
             e = launch_plan(cu_seqlens, num_seqs, total_tokens, kChunk, chunk_off, st, s);
             if (e == cudaSuccess)
                 e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
-                                    slots, H, initial_state, S_run, o, ws + rec_off, window, st,
-                                    s, nullptr);
+                                    slots, H, initial_state, S_run, o, ws + rec_off, window, 1,
+                                    st, s, nullptr);
         } else {
             e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
                                   total_tokens, H, initial_state, final_state, o, st, s,

@@ -151,7 +151,8 @@ def chunk_fwd_profiled(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, fi
     """kda_chunk_fwd with CUDA events recorded around each kernel it launches.
 
     `events` is a list of torch.cuda.Event(enable_timing=True); returns how many
-    were recorded (events[0] before the first kernel, events[i] after the i-th).
+    were recorded.  Kernel j of the call runs between events[2j] and events[2j+1],
+    both recorded on the stream that kernel was launched on.
     """
     lib = load()
     _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)

@@ -86,6 +86,15 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
  * Sequence Bottleneck").  The result equals the token-by-token recurrence
  * up to rounding.
  *
+ * Work is enqueued on `stream` and returns without synchronising.  On the
+ * tensor-core path (bf16, dk = dv = 128) a problem with more than one window
+ * of chunk records also runs kernels on streams the library owns (created on
+ * first use per device, kept for the life of the process): they start after
+ * everything enqueued on `stream` before the call, and `stream` waits for them
+ * before anything enqueued after it, so to the caller the call behaves as work
+ * on `stream` alone.  Calls from several host threads are serialised while
+ * they enqueue.
+ *
  *   q, k, z       [total_tokens, H, dk]  dtype
  *   v             [total_tokens, H, dv]  dtype
  *   beta          [total_tokens, H]      dtype
@@ -109,10 +118,11 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
 /*
  * kda_chunk_fwd with per-kernel timing: identical arguments and results, plus
  * `events`, an array of n_events caller-created cudaEvent_t handles (created
- * with timing enabled).  The call records events[0] on `stream` before its
- * first kernel and events[i] after its i-th kernel, for as many kernels as fit,
- * and writes the number of events recorded to *n_recorded (host pointer).  The
- * kernels of one call on the tensor-core path are, in order: the chunk plan,
+ * with timing enabled).  The call brackets its j-th kernel with events[2j]
+ * (before) and events[2j+1] (after), both recorded on the stream that kernel is
+ * launched on, for as many kernels as fit, and writes the number of events
+ * recorded to *n_recorded (host pointer).  The kernels of one call on the
+ * tensor-core path are, in launch order: the chunk plan,
  * the running-state initialisation (absent when initial_state aliases
  * final_state), then one (prep, chain) pair per window of chunk records; on
  * the CUDA-core path, one chunked kernel.  Used by the benchmark to time the

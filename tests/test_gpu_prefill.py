@@ -114,3 +114,40 @@ def test_both_chain_shapes(lens):
     d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=len(lens),
                             h0_sigma=0.1, device=DEV)
     _run_and_score(d, "bf16")
+
+
+def test_profiled_entry_pairs_and_stream_order():
+    """kda_chunk_fwd_profiled brackets each kernel with an event pair and gives the same
+    results as kda_chunk_fwd; inputs written on a side stream just before the call, and
+    outputs read on it right after, see the call's work in order (the call may run
+    kernels on the library's own streams)."""
+    # more than one window of chunk records (1 GiB), so that the double-buffered schedule
+    # with its own streams runs
+    d = inputs.make_prefill([20000, 4000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
+                            h0_sigma=0.1, device=DEV)
+    T, H, dk = d["q"].shape
+    N = 2
+    ws_bytes = kda.chunk_fwd_workspace_size(T, N, H, dk, 128, torch.bfloat16)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        q2 = torch.empty_like(d["q"])
+        ws = kda.alloc_workspace(ws_bytes, DEV)
+        o = torch.full((T, H, 128), float("nan"), dtype=torch.bfloat16, device=DEV)
+        hT = torch.empty(N, H, dk, 128, dtype=torch.float32, device=DEV)
+        o2, hT2 = torch.empty_like(o), torch.empty_like(hT)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(256)]
+        for _ in range(3):          # a slow producer of the input on the side stream
+            q2.copy_(d["q"] * 1.0)
+        used = kda.chunk_fwd_profiled(q2, d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                                      d["cu_seqlens"], d["h0"], o, hT, ws, ev, stream=side)
+        o_host = o.float().cpu()    # ordered after the call on the side stream
+        kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
+                      d["h0"], o=o2, final_state=hT2, workspace=ws, stream=side)
+    side.synchronize()
+    assert used >= 2 * (2 + 2 * 2) and used % 2 == 0   # plan, init, two (prep, chain) pairs
+    assert all(ev[j].elapsed_time(ev[j + 1]) >= 0.0 for j in range(0, used, 2))
+    assert not torch.isnan(o_host).any()
+    assert torch.equal(o, o2) and torch.equal(hT, hT2)
+    e_o, e_s = score_prefill(d, o, hT, None, [0, 17, 31])
+    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"]

@@ -54,7 +54,7 @@ constexpr uint32_t REC_G = 90112;
 constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
-constexpr int PREP_THREADS = 512;
+constexpr int PREP_THREADS = 256;
 constexpr int PREP_WARPS = PREP_THREADS / 32;
 constexpr int NU = 32 / PREP_WARPS;     // 8-channel units per thread in the element-wise passes
 constexpr int CHG = 2 * NU;             // 8-channel chunks per warp (per half-warp: NU)
@@ -580,6 +580,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 }
 
 // ---------------------------------------------------------------- chain kernels
+// Records of chunks this far ahead of the one being walked are pulled into L2.
+constexpr int kPrefetchAhead = 3;
 // largest n in [0, N) with chunk_off[n] <= slot (the owner of a used slot)
 __device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32_t slot) {
     int lo = 0, hi = N - 1;
@@ -777,6 +779,13 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     chain_load(sm + (b ^ 1) * BUF_BYTES,
                                records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
                                &bar[b ^ 1]);
+                // and the parts of the record kPrefetchAhead chunks on that this CTA reads
+                if (tid == 64 && cs + kPrefetchAhead < c_end) {
+                    const uint8_t *r2 = records + ((size_t)(cs + kPrefetchAhead - slot0) * H + h) * REC_BYTES;
+                    bulk_prefetch_l2(r2 + REC_WQ, REC_U - REC_WQ);
+                    bulk_prefetch_l2(r2 + REC_U + blk * 8192, 8192);
+                    bulk_prefetch_l2(r2 + REC_G, REC_BYTES - REC_G);
+                }
             }
             if (!ok) *abort_flag = 1;
             fence_proxy_async();
@@ -1025,6 +1034,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     chain_load(sm + buf_off(b ^ 1),
                                records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES,
                                &bar[b ^ 1]);
+                // and the record kPrefetchAhead chunks on
+                if (tid == 64 && cs + kPrefetchAhead < c_end)
+                    bulk_prefetch_l2(records + ((size_t)(cs + kPrefetchAhead - slot0) * H + h) * REC_BYTES,
+                                     REC_BYTES);
             }
             if (!ok) *abort_flag = 1;
             fence_proxy_async();

@@ -65,7 +65,6 @@ constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and
 // CTAs fit on one SM.  Regions are reused once the A/P products have completed.
 constexpr uint32_t P_BAR = 0;           // 2 mbarriers, TMEM slot
 constexpr uint32_t P_TOT = 1024;        // fp32 [4][128]  per-tile sums of g
-constexpr uint32_t P_REF = 3072;        // fp32 [5][128]  ref_0..ref_3 (cumsum before tile a), G_C
 constexpr uint32_t P_ER = 5632;         // fp32 [4][128]  exp(ref_a)
 constexpr uint32_t P_RT = 7680;         // fp32 [6][128]  exp(ref_a' - ref_a), a < a'
 constexpr uint32_t P_KTF = 10752;       // fp32 [4][128]  exp(G_C - ref_a)
@@ -79,6 +78,9 @@ constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64
 constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
 constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
+constexpr uint32_t P_NS = 1024;         // (solve) fp32 N_ab blocks [6][16][16] over the dead tables
+constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
+constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, fp32 [4][64][32]
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
 constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
 constexpr uint32_t P_SMEM = P_END + 1024;
@@ -86,6 +88,8 @@ static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K image
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
 static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
+static_assert(P_NS + 6 * 256 * 4 <= P_BETA && P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB,
+              "solve / epilogue staging overlaps live data");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
@@ -151,7 +155,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     uint8_t *rec = records + ((size_t)blockIdx.x * H + h) * REC_BYTES;
 
     float *TOT = reinterpret_cast<float *>(sm + P_TOT);
-    float *REF = reinterpret_cast<float *>(sm + P_REF);
     float *ER = reinterpret_cast<float *>(sm + P_ER);
     float *RT = reinterpret_cast<float *>(sm + P_RT);
     float *KTF = reinterpret_cast<float *>(sm + P_KTF);
@@ -256,11 +259,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             ref[t] = run;
-            REF[t * DK + c] = run;
             ER[t * DK + c] = expf(run);
             run += TOT[t * DK + c];
         }
-        REF[4 * DK + c] = run;
         *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
 #pragma unroll
         for (int t = 0; t < 4; ++t) KTF[t * DK + c] = expf(run - ref[t]);
@@ -405,6 +406,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
     //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
+    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E) is written as the
+    // blocks of T appear: diagonal blocks here, zero blocks above the diagonal by the other
+    // threads, the blocks below it at the end of the solve.
+    float *NS = reinterpret_cast<float *>(sm + P_NS);   // N_ab blocks [pair][16][16]
+    uint8_t *TBI = sm + P_TB;
     if (tid < 64) {  // diagonal blocks T_aa = (I + A_aa)^-1: thread (block tb, column j)
         const int tb = tid >> 4, j = tid & 15;
         float tcol[16];
@@ -413,10 +419,22 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             float s = (i == j) ? 1.f : 0.f;
 #pragma unroll
             for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * LDA + 16 * tb + m] * tcol[m];
-            tcol[i] = s;
+            tcol[i] = s;   // zero above the diagonal
         }
+        const float bj = BETA[16 * tb + j];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
+        for (int i = 0; i < 16; ++i) {
+            TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
+            *reinterpret_cast<__nv_bfloat16 *>(TBI + sw128_offset(16 * tb + i, 16 * tb + j, 64)) =
+                __float2bfloat16_rn(tcol[i] * bj);
+        }
+    } else if (tid < 64 + 192) {
+        // blocks (a, b > a): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 16 rows x two 16-byte chunks
+        const int e = tid - 64, ub = e >> 5, rc = e & 31;
+        const int ua = ub < 3 ? 0 : (ub < 5 ? 1 : 2);
+        const int uc = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
+        *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64)) =
+            make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
@@ -433,43 +451,34 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             x.x += xv * y.x; x.y += xv * y.y; x.z += xv * y.z; x.w += xv * y.w;
         }
     };
-    // N_ab = T_aa A_ab, in place over A (all reads happen before the barrier)
-    {
-        float4 nv[SOLVE_W];
+    // N_ab = T_aa A_ab
 #pragma unroll
-        for (int w = 0; w < SOLVE_W; ++w) {
-            const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
-            nv[w] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (task < 384) {
-                const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
-                const int a2 = pair_a(pr), b = pair_b(pr);
-                acc16(nv[w], TS + (16 * a2 + i) * LDA + 16 * a2, AS + (16 * a2) * LDA + 16 * b + 4 * jq, LDA);
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int w = 0; w < SOLVE_W; ++w) {
-            const int task = tid + w * PREP_THREADS;
-            if (task < 384) {
-                const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
-                *reinterpret_cast<float4 *>(AS + (16 * pair_a(pr) + i) * LDA + 16 * pair_b(pr) + 4 * jq) = nv[w];
-            }
+    for (int w = 0; w < SOLVE_W; ++w) {
+        const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
+        if (task < 384) {
+            const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
+            const int a2 = pair_a(pr), b = pair_b(pr);
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            acc16(x, TS + (16 * a2 + i) * LDA + 16 * a2, AS + (16 * a2) * LDA + 16 * b + 4 * jq, LDA);
+            *reinterpret_cast<float4 *>(NS + pr * 256 + i * 16 + 4 * jq) = x;
         }
     }
     __syncthreads();
     float *XS = reinterpret_cast<float *>(sm + P_XS);   // [0] N2_20 [1] N2_31 [2] N2_30 [3] N3_30
-    auto nrow = [&](int a2, int b, int i) { return AS + (16 * a2 + i) * LDA + 16 * b; };
+    // N_ab row i, and the 4-column group jq of N_ab, for pair numbers p
+    auto nrow = [&](int p, int i) { return NS + p * 256 + i * 16; };
+    auto ncol = [&](int p, int jq) { return NS + p * 256 + 4 * jq; };
     if (tid < 192) {
         // N^2 blocks: (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20 (warp-uniform q)
         const int q = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q == 0) {
-            acc16(x, nrow(2, 1, i), AS + 16 * LDA + 4 * jq, LDA);
+            acc16(x, nrow(1, i), ncol(0, jq), 16);
         } else if (q == 1) {
-            acc16(x, nrow(3, 2, i), AS + 32 * LDA + 16 + 4 * jq, LDA);
+            acc16(x, nrow(2, i), ncol(1, jq), 16);
         } else {
-            acc16(x, nrow(3, 1, i), AS + 16 * LDA + 4 * jq, LDA);
-            acc16(x, nrow(3, 2, i), AS + 32 * LDA + 4 * jq, LDA);
+            acc16(x, nrow(4, i), ncol(0, jq), 16);
+            acc16(x, nrow(2, i), ncol(3, jq), 16);
         }
         *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
     }
@@ -477,11 +486,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (tid < 64) {  // N^3_30 = N32 N^2_20
         const int i = tid >> 2, jq = tid & 3;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc16(x, nrow(3, 2, i), XS + 4 * jq, 16);
+        acc16(x, nrow(2, i), XS + 4 * jq, 16);
         *reinterpret_cast<float4 *>(XS + 3 * 256 + i * 16 + 4 * jq) = x;
     }
     __syncthreads();
-    // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise)
+    // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise), scaled by b and written to the image
 #pragma unroll
     for (int w = 0; w < SOLVE_W; ++w) {
         const int task = tid + w * PREP_THREADS;
@@ -490,7 +499,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             const int a2 = pair_a(pr), b = pair_b(pr);
             const int n2 = pr == 3 ? 0 : pr == 4 ? 1 : pr == 5 ? 2 : -1;
             float mrow[16];
-            const float *nr = nrow(a2, b, i);
+            const float *nr = nrow(pr, i);
 #pragma unroll
             for (int t = 0; t < 16; ++t) mrow[t] = -nr[t];
             if (n2 >= 0) {
@@ -503,20 +512,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             }
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             acc16(x, mrow, TS + (16 * b) * LDA + 16 * b + 4 * jq, LDA);
-            *reinterpret_cast<float4 *>(TS + (16 * a2 + i) * LDA + 16 * b + 4 * jq) = x;
+            const float4 bb = *reinterpret_cast<const float4 *>(BETA + 16 * b + 4 * jq);
+            uint2 pk;
+            *reinterpret_cast<__nv_bfloat162 *>(&pk.x) = __floats2bfloat162_rn(x.x * bb.x, x.y * bb.y);
+            *reinterpret_cast<__nv_bfloat162 *>(&pk.y) = __floats2bfloat162_rn(x.z * bb.z, x.w * bb.w);
+            *reinterpret_cast<uint2 *>(TBI + sw128_offset(16 * a2 + i, 16 * b + 4 * jq, 64)) = pk;
         }
-    }
-    __syncthreads();
-    // T diag(b) as the K-major [64][64] A image, 16-byte stores (upper part zero)
-    for (int e = tid; e < C * 8; e += PREP_THREADS) {
-        const int rr = e >> 3, j8 = (e & 7) * 8;
-        float x[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int j = j8 + i;
-            x[i] = (j <= rr) ? TS[rr * LDA + j] * BETA[j] : 0.f;
-        }
-        *reinterpret_cast<uint4 *>(sm + P_TB + sw128_offset(rr, j8, 64)) = pack8(x);
     }
     fence_proxy_async();
     tc_fence_before();
@@ -536,9 +537,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (F) W rows -> record WQ rows 0..63; Ut -> record fp32.  Rows 0..63 live in lane
-    //          quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut) x
-    //          (32-column block), two 16-column TMEM loads in flight per wait
+    // ---- (F) W rows (K-major, rows 0..63 of the record's WQ image) and Ut (fp32) are staged
+    //          in the freed shared memory and leave in three bulk copies.  Rows 0..63 live in
+    //          lane quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut)
+    //          x (32-column block), two 16-column TMEM loads in flight per wait.
+    uint8_t *WST = sm + P_WST;   // [2 K halves][64 rows][128 B]
+    uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] fp32, slots swizzled
     if ((warp & 3) < 2) {
         const int quarter = warp & 3;
         const int rr = 32 * quarter + lane;
@@ -556,12 +560,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                     float x[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = i8 < 2 ? lo[8 * i8 + i] : hi[8 * (i8 - 2) + i];
-                    *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(rr, 32 * cb + 8 * i8, 128)) = pack8(x);
+                    *reinterpret_cast<uint4 *>(WST + sw128_offset(rr, 32 * cb + 8 * i8, 64)) = pack8(x);
                 }
             } else {
                 // row rr of column block cb; float4 j4 stored at slot j4 ^ (rr % 8) so that the
                 // chain kernel's row-per-thread reads hit distinct banks
-                float4 *dst = reinterpret_cast<float4 *>(rec + REC_U + ((cb * 64 + rr) * 32) * 4);
+                float4 *dst = reinterpret_cast<float4 *>(UST + ((cb * 64 + rr) * 32) * 4);
 #pragma unroll
                 for (int i4 = 0; i4 < 8; ++i4) {
                     const float *v4 = i4 < 4 ? lo + 4 * i4 : hi + 4 * (i4 - 4);
@@ -570,12 +574,20 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             }
         }
     }
+    fence_proxy_async();
     if (!ok && tid == 0) report(st, KDA_ERR_TIMEOUT, slot, 10);
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
+        if (lane == 0) {
+            bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
+            bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
+            bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
+            bulk_commit();
+            bulk_wait_all();
+        }
     }
 }
 

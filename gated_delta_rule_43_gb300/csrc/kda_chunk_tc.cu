@@ -79,6 +79,8 @@ constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
 constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
 constexpr uint32_t P_NS = 1024;         // (solve) fp32 N_ab blocks [6][16][16] over the dead tables
+constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], before N
+constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
 constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
 constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, fp32 [4][64][32]
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
@@ -88,7 +90,8 @@ static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K image
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
 static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
-static_assert(P_NS + 6 * 256 * 4 <= P_BETA && P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB,
+static_assert(P_NS + 6 * 256 * 4 <= P_BETA && P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
+                  P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
               "solve / epilogue staging overlaps live data");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -302,7 +305,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const uint32_t row = 32 * a + rl;
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row, c, 128)) = pack8(kr);
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
-        *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(64 + r, c, 128)) = pack8(qg);
+        *reinterpret_cast<uint4 *>(sm + P_QST + sw128_offset(r, c, 64)) = pack8(qg);
         *reinterpret_cast<uint4 *>(rec + REC_KT + sw128_offset(r, c, 64)) = pack8(kt);
         // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a);
         // image a2 occupies rows 8 a2 (a2 + 1) .. of the stacked [160][128] B operand
@@ -333,6 +336,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             umma_bf16(tmem, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
                       desc_add(bd, (s >> 2) * KC_ROWS * 128 + (s & 3) * 32), idesc, s > 0);
         umma_commit(&bar[0]);
+        // Q*Gam (staged in pass B) -> rows 64..127 of the record's WQ image, both K halves
+        bulk_s2g(rec + REC_WQ + 8192, sm + P_QST, 8192);
+        bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
+        bulk_commit();
     }
     // prefetch this thread's V chunks while the products run
     uint4 vv[NU];
@@ -395,13 +402,19 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                         const int j = 16 * m + 8 * half + i;
                         x[i] = (j <= rr) ? val[mm][8 * half + i] : 0.f;
                     }
-                    *reinterpret_cast<uint4 *>(rec + REC_P + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
+                    *reinterpret_cast<uint4 *>(sm + P_PST + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
                 }
             }
         }
     }
+    if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
+    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {                       // P -> the record
+        bulk_s2g(rec + REC_P, sm + P_PST, 8192);
+        bulk_commit();
+    }
 
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
@@ -436,6 +449,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64)) =
             make_uint4(0, 0, 0, 0);
     }
+    if (tid == 0) bulk_wait_read_all();   // the P staging (under the N blocks) is free
     __syncthreads();
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
     // The diagonal blocks of T hold explicit zeros above the diagonal, so every product

@@ -58,7 +58,7 @@ constexpr int PREP_THREADS = 256;
 constexpr int PREP_WARPS = PREP_THREADS / 32;
 constexpr int NU = 32 / PREP_WARPS;     // 8-channel units per thread in the element-wise passes
 constexpr int CHG = 2 * NU;             // 8-channel chunks per warp (per half-warp: NU)
-constexpr int SOLVE_W = (384 + PREP_THREADS - 1) / PREP_THREADS;   // solve tasks per thread
+constexpr int SOLVE_W = (384 + 128 + PREP_THREADS - 1) / PREP_THREADS;   // solve tasks per thread
 static_assert(PREP_WARPS == 8 || PREP_WARPS == 16, "prep kernel runs 8 or 16 warps");
 constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and T tiles
 // Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
@@ -407,7 +407,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             }
         }
     }
-    if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -419,9 +418,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
     //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
-    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E) is written as the
-    // blocks of T appear: diagonal blocks here, zero blocks above the diagonal by the other
-    // threads, the blocks below it at the end of the solve.
+    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E) shares its region
+    // with the Q*Gam staging, whose bulk copy is given until the N^3 step to finish; it is
+    // written there: zero blocks above the diagonal in the N^3 step, the other blocks in
+    // the last step of the solve.
     float *NS = reinterpret_cast<float *>(sm + P_NS);   // N_ab blocks [pair][16][16]
     uint8_t *TBI = sm + P_TB;
     if (tid < 64) {  // diagonal blocks T_aa = (I + A_aa)^-1: thread (block tb, column j)
@@ -434,20 +434,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * LDA + 16 * tb + m] * tcol[m];
             tcol[i] = s;   // zero above the diagonal
         }
-        const float bj = BETA[16 * tb + j];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
-            *reinterpret_cast<__nv_bfloat16 *>(TBI + sw128_offset(16 * tb + i, 16 * tb + j, 64)) =
-                __float2bfloat16_rn(tcol[i] * bj);
-        }
-    } else if (tid < 64 + 192) {
-        // blocks (a, b > a): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 16 rows x two 16-byte chunks
-        const int e = tid - 64, ub = e >> 5, rc = e & 31;
-        const int ua = ub < 3 ? 0 : (ub < 5 ? 1 : 2);
-        const int uc = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
-        *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64)) =
-            make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
     }
     if (tid == 0) bulk_wait_read_all();   // the P staging (under the N blocks) is free
     __syncthreads();
@@ -496,12 +484,20 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
     }
+    if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
     __syncthreads();
     if (tid < 64) {  // N^3_30 = N32 N^2_20
         const int i = tid >> 2, jq = tid & 3;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         acc16(x, nrow(2, i), XS + 4 * jq, 16);
         *reinterpret_cast<float4 *>(XS + 3 * 256 + i * 16 + 4 * jq) = x;
+    } else if (tid < 64 + 192) {
+        // zero blocks (a, b > a): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 16 rows x two 16-byte chunks
+        const int e = tid - 64, ub = e >> 5, rc = e & 31;
+        const int ua = ub < 3 ? 0 : (ub < 5 ? 1 : 2);
+        const int uc = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
+        *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64)) =
+            make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise), scaled by b and written to the image
@@ -531,6 +527,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             *reinterpret_cast<__nv_bfloat162 *>(&pk.x) = __floats2bfloat162_rn(x.x * bb.x, x.y * bb.y);
             *reinterpret_cast<__nv_bfloat162 *>(&pk.y) = __floats2bfloat162_rn(x.z * bb.z, x.w * bb.w);
             *reinterpret_cast<uint2 *>(TBI + sw128_offset(16 * a2 + i, 16 * b + 4 * jq, 64)) = pk;
+        } else if (task < 384 + 128) {
+            // diagonal blocks: (block tb, row i, 8-column half) -> one 16-byte chunk
+            const int e = task - 384, tb = e >> 5, i = (e >> 1) & 15, hf = e & 1;
+            float x[8], bt[8], tt[8];
+            ld8(TS + (16 * tb + i) * LDA + 16 * tb + 8 * hf, tt);
+            ld8(BETA + 16 * tb + 8 * hf, bt);
+#pragma unroll
+            for (int c = 0; c < 8; ++c) x[c] = tt[c] * bt[c];
+            *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * tb + i, 16 * tb + 8 * hf, 64)) = pack8(x);
         }
     }
     fence_proxy_async();

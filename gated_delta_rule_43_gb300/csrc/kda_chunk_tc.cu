@@ -631,7 +631,7 @@ namespace c32 {
 
 constexpr int DVB = 32;          // value columns per CTA
 constexpr int NBLK = DV / DVB;
-constexpr int CHAIN_THREADS = 128;
+constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [0; P] U
 constexpr uint32_t B_WQ = 0, B_KT = 32768, B_ZP = 49152, B_U = 65536, B_G = 73728;
 constexpr uint32_t BUF_BYTES = 74752;
 constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
@@ -678,7 +678,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
              float *__restrict__ state, __nv_bfloat16 *__restrict__ o, StatusWord *st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t used = min(slot1, chunk_off[N]);
     if (slot0 >= used) return;
     const int n_first = slot_owner(chunk_off, N, slot0);
@@ -730,13 +730,15 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         const int j0 = blk * DVB;
         float S[DVB];
         float *srow = state + (((int64_t)n * H + h) * DK + i) * DV + j0;
+        if (warp < 4) {
 #pragma unroll
-        for (int j4 = 0; j4 < DVB / 4; ++j4) {
-            const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
-            S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+            for (int j4 = 0; j4 < DVB / 4; ++j4) {
+                const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
+                S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+            }
+            store_row_sw64(sm + C_S, i, S);
+            fence_proxy_async();
         }
-        store_row_sw64(sm + C_S, i, S);
-        fence_proxy_async();
         __syncthreads();
         if (tid == 0)
             chain_load(sm + (gi & 1) * BUF_BYTES,
@@ -800,9 +802,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                         acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
                         acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
                     }
+                    // the U image is free once the previous chunk's [0; P] U product is done
+                    if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                     store_row_sw64(sm + C_UI, r, acc);
                 }
-            } else {
+            } else if (warp < 4) {
                 // previous chunk's outputs, off the critical path; its [0; P] U product was
                 // the last reader of the other buffer, which then takes the next chunk
                 if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
@@ -831,16 +835,20 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 for (int s = 0; s < C / 16; ++s)
                     umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
                 umma_commit(&bar[3]);
-                // ... then D1[b] += [0; P] U (outputs only), which runs while S is updated
-                const uint64_t azp = sdesc_sw128(bufa + B_ZP, 16, 1024);
-#pragma unroll
-                for (int s = 0; s < C / 16; ++s)
-                    umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024), id_km, 1);
-                umma_commit(&bar[4]);
             }
             ok = mbar_wait(&bar[3], gi & 1);
             tc_fence_after();
-            if (ok) {
+            if (warp == 4) {
+                // ... then D1[b] += [0; P] U (outputs only), issued by warp 4 behind D2 so
+                // that it runs while S is updated
+                if (lane == 0 && ok) {
+                    const uint64_t azp = sdesc_sw128(bufa + B_ZP, 16, 1024);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024), id_km, 1);
+                    umma_commit(&bar[4]);
+                }
+            } else if (ok) {
                 // S <- Diag(Gam_C) S + D2 (row i = tid)
                 const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
                 float acc[32];
@@ -862,12 +870,14 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         } else {
             tc_fence_after();
             bool ok_o = true;
-            if (warp >= 2) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (warp >= 2 && warp < 4) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
             if (!ok_o) *abort_flag = 1;
+            if (warp < 4) {
 #pragma unroll
-            for (int j4 = 0; j4 < DVB / 4; ++j4)
-                reinterpret_cast<float4 *>(srow)[j4] =
-                    make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
+                for (int j4 = 0; j4 < DVB / 4; ++j4)
+                    reinterpret_cast<float4 *>(srow)[j4] =
+                        make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
+            }
         }
         tc_fence_before();
         __syncthreads();

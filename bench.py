@@ -38,6 +38,26 @@ PREFILL = "prefill_8k"
 DECODE = "decode_256"
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
+
+
+def profiled_traffic(md_name: str):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, or None when
+    the kernel sources it names have changed since the capture."""
+    import hashlib
+    try:
+        text = open(os.path.join(ROOT, "profiles", md_name)).read()
+        fields = dict(line.strip().split(": ", 1) for line in text.splitlines()
+                      if line.strip().split(": ", 1)[0] in
+                      ("traffic_bytes_per_launch", "source_sha256_16", "sources"))
+        h = hashlib.sha256()
+        for f in fields["sources"].split():
+            with open(os.path.join(ROOT, f), "rb") as fh:
+                h.update(fh.read())
+        if h.hexdigest()[:16] != fields["source_sha256_16"]:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
 # fallbacks only when the measured peaks file is absent
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -269,7 +289,9 @@ def run_ours(args, rank, world, local):
                    "l2": "flushed between timed steps (256 MiB write outside the events)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved_gbs / hbm_peak, "traffic": None,
+                     "frac": achieved_gbs / hbm_peak,
+                     "traffic": (profiled_traffic(f"{dom}_prefill_8k.md")
+                                 if dom in ("prep_kernel", "chain_kernel") else None),
                      "kernel": dom, "peak_source": pk_src,
                      "algorithmic_bytes_per_launch": algo_bytes / launches[dom],
                      "launches_per_step": launches[dom],
@@ -336,7 +358,8 @@ def decode_bench(args, dev, stream, world, pk, pk_src):
             "value": agg, "unit": "state GB/s", "median_step_us": med * 1e6,
             "state_gbs_median_step": gbs_state, "steps": steps,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                         "frac": achieved / hbm, "traffic": None,
+                         "frac": achieved / hbm,
+                         "traffic": profiled_traffic("decode_step_kernel_decode_256.md"),
                          "kernel": "decode_step_kernel", "peak_source": pk_src,
                          "algorithmic_bytes_per_launch": state_bytes + io_bytes},
             "gpu_launches": steps}

@@ -366,50 +366,68 @@ def decode_bench(args, dev, stream, world, pk, pk_src):
 
 
 def e2e_bench(args, d, dev, stream, world):
-    """Same prefill metric through the public call with pinned host buffers:
-    H2D of every input and D2H of o and the final state inside the timed region."""
+    """Same prefill metric through the public call with pinned host buffers: H2D of every
+    input and D2H of o and the final state inside the timed region, every step.  Steps
+    alternate between two streams with their own device buffers, so that the copies of
+    one step overlap the compute of the other (what a caller streaming batches does)."""
     import torch
 
     from gated_delta_rule_43_gb300 import kda
 
     names = ("q", "k", "v", "z", "beta", "A_log", "cu_seqlens")
     host = {n: d[n].cpu().pin_memory() for n in names}
-    devb = {n: torch.empty_like(d[n]) for n in names}
     T, H, dv = d["v"].shape
     N = d["cu_seqlens"].numel() - 1
     dk = d["q"].shape[2]
-    o = torch.empty(T, H, dv, dtype=d["q"].dtype, device=dev)
-    hT = torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev)
-    o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-    s_h = torch.empty(hT.shape, dtype=torch.float32).pin_memory()
-    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, N, H, dk, dv, o.dtype), dev)
-    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = o.numel() * o.element_size() + hT.numel() * 4
-
-    def step():
-        for n in names:
-            devb[n].copy_(host[n], non_blocking=True)
-        kda.chunk_fwd(devb["q"], devb["k"], devb["v"], devb["z"], devb["beta"], devb["A_log"],
-                      devb["cu_seqlens"], None, o=o, final_state=hT, workspace=ws,
-                      stream=stream)
-        o_h.copy_(o, non_blocking=True)
-        s_h.copy_(hT, non_blocking=True)
-
+    ws_bytes = kda.chunk_fwd_workspace_size(T, N, H, dk, dv, d["q"].dtype)
+    lanes = []
     for _ in range(2):
-        step()
+        lanes.append({
+            "s": torch.cuda.Stream(dev),
+            "dev": {n: torch.empty_like(d[n]) for n in names},
+            "o": torch.empty(T, H, dv, dtype=d["q"].dtype, device=dev),
+            "hT": torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev),
+            "o_h": torch.empty((T, H, dv), dtype=d["q"].dtype).pin_memory(),
+            "s_h": torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory(),
+            "ws": kda.alloc_workspace(ws_bytes, dev),
+        })
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = lanes[0]["o"].numel() * lanes[0]["o"].element_size() + lanes[0]["hT"].numel() * 4
+
+    def step(i):
+        L = lanes[i % 2]
+        with torch.cuda.stream(L["s"]):
+            for n in names:
+                L["dev"][n].copy_(host[n], non_blocking=True)
+            b = L["dev"]
+            kda.chunk_fwd(b["q"], b["k"], b["v"], b["z"], b["beta"], b["A_log"], b["cu_seqlens"],
+                          None, o=L["o"], final_state=L["hT"], workspace=L["ws"], stream=L["s"])
+            L["o_h"].copy_(L["o"], non_blocking=True)
+            L["s_h"].copy_(L["hT"], non_blocking=True)
+
+    for i in range(2):
+        step(i)
     torch.cuda.synchronize(dev)
-    K = max(3, args.steps // 2)
+    K = max(4, args.steps)
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for _ in range(K):
-        step()
+    for L in lanes:
+        L["s"].wait_stream(stream)
+    for i in range(K):
+        step(i)
+    for L in lanes:
+        stream.wait_stream(L["s"])
     e.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
+    for L in lanes:
+        kda.query_status(L["ws"], raise_on_error=True)
     val, _ = aggregate(T * K, s.elapsed_time(e) / 1e3, world)
     return {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-            "d2h_bytes_per_step": d2h, "steps": K}
+            "d2h_bytes_per_step": d2h, "steps": K,
+            "note": "two streams, double-buffered device inputs: copies of one step overlap "
+                    "the compute of the next"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -21,7 +21,7 @@ cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t 
 size_t tc_record_bytes();
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
-                            const int32_t *chunk_off, int N, int64_t slots, int H,
+                            const int32_t *chunk_off, int N, int64_t T_tot, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec);
@@ -122,6 +122,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
     const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype);
     if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
     if (chunk_slots_overflow(total_tokens, num_seqs, kTcChunk)) return KDA_ERR_INVALID_ARG;
+    // token coordinates of the tensor-core path's tile loads are 32-bit
+    if (use_tc(dtype, dk, dv) && total_tokens >= ((int64_t)1 << 31)) return KDA_ERR_INVALID_ARG;
 
     cudaStream_t s = (cudaStream_t)stream;
     StatusWord *st = (StatusWord *)workspace;
@@ -136,7 +138,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
         e = launch_plan(cu_seqlens, num_seqs, total_tokens, kTcChunk, chunk_off, st, s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
         if (rec) rec->mark(s);
-        e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs, L.slots, H,
+        e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
+                            total_tokens, L.slots, H,
                             initial_state, S_run, o, ws + L.rec_off, L.window, L.nbuf, st, s,
                             rec);
         return cuda_status(e);

@@ -31,6 +31,9 @@
 //   P   K-major [64][64]
 //   Ut  fp32 [4 column blocks][64][32], float4 slot j4 of row r holds columns 4 (j4 ^ (r % 8))
 //   GC  fp32 [128] Gam_C
+#include <cuda.h>
+#include <string.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -146,7 +149,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
-            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st, int ahead) {
+            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st, int ahead,
+            const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -164,6 +168,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     float *BETA = reinterpret_cast<float *>(sm + P_BETA);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_BAR + 16);
+    uint64_t *vbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 32);   // the V tile's TMA
 
     const int a = warp & 3;                    // this thread's 16-token tile
     const int rl = lane & 15;
@@ -209,6 +214,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
+        mbar_init(vbar, 1);
         fence_mbar_init();
     }
 
@@ -341,23 +347,20 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
         bulk_commit();
     }
-    // prefetch this thread's V chunks while the products run
-    uint4 vv[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int ch = CHG * (warp >> 2) + 2 * u + (lane >> 4);
-        vv[u] = valid ? *reinterpret_cast<const uint4 *>(v + ((t0 + r) * H + h) * (int64_t)DV + 8 * ch)
-                      : make_uint4(0, 0, 0, 0);
-    }
     bool ok = mbar_wait(&bar[0], 0);
     tc_fence_after();
-
-    // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region
+    // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region: the V half arrives
+    //          by TMA (two 64-channel boxes of 64 tokens, 128-byte swizzle, which is the
+    //          operand layout) and is not needed before step E; K*Gam from registers
+    if (tid == 0) {
+        mbar_arrive_expect_tx(vbar, 2 * 64 * 128);
+        tma_load_3d(sm + P_KGV + 2 * 8192, &tmap_v, 0, h, (int32_t)t0, vbar);
+        tma_load_3d(sm + P_KGV + 3 * 8192, &tmap_v, 64, h, (int32_t)t0, vbar);
+    }
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
         const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = kgam[u];
-        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, 128 + c, 64)) = vv[u];
     }
     // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
     // warp w reads its own lane quarter t = w & 3 (rows 32t.. of D_t: 16 Kr rows, then
@@ -538,12 +541,23 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * tb + i, 16 * tb + 8 * hf, 64)) = pack8(x);
         }
     }
+    if (L < C) {
+        // a sequence's last chunk: the V box also holds the next rows of the tensor; zero the
+        // rows past the sequence end so that nothing of another sequence reaches U~
+        ok = mbar_wait(vbar, 0) && ok;
+        for (int e = tid; e < (C - L) * 16; e += PREP_THREADS) {
+            const int rr = L + (e >> 4), c8 = e & 15;
+            *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(rr, 128 + 8 * c8, 64)) =
+                make_uint4(0, 0, 0, 0);
+        }
+    }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
 
     // ---- (E) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
     if (tid == 0) {
+        ok = mbar_wait(vbar, 0) && ok;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 256, false, true);
         const uint64_t ad = sdesc_sw128(base + P_TB, 16, 1024);
@@ -1191,19 +1205,61 @@ cudaError_t pipe_setup(int dev, Pipe *&out) {
     return e;
 }
 
-}  // namespace
-
 // Records: nbuf (1 or 2) buffers of `window` chunk slots x H records each.  With one
 // buffer the windows run prep, chain, prep, chain ... on `s`.  With two, prep of
 // window w + 1 runs beside chain of window w (see Pipe); the call's work is still
 // ordered after everything enqueued on `s` before it and before everything after it.
+// cuTensorMapEncodeTiled, reached through the runtime's entry-point query (the library
+// links no driver library)
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+}  // namespace
+
+// Tensor map of a [T_tot, H, 128] bf16 tensor read in boxes of 64 tokens x 1 head x 64
+// channels with the 128-byte swizzle (the MN-major operand layout of the prep kernel).
+static cudaError_t tmap_thd(CUtensorMap *m, const void *x, int64_t T_tot, int H) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[3] = {128, (cuuint64_t)H, (cuuint64_t)T_tot};
+    const cuuint64_t strides[2] = {128 * 2, (cuuint64_t)H * 128 * 2};
+    const cuuint32_t box[3] = {64, 1, 64};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(x), dims,
+                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
-                            const int32_t *chunk_off, int N, int64_t slots, int H,
+                            const int32_t *chunk_off, int N, int64_t T_tot, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec) {
     using namespace tc;
+    CUtensorMap tmap_v;
+    if (T_tot > 0) {
+        cudaError_t te = tmap_thd(&tmap_v, v, T_tot, H);
+        if (te != cudaSuccess) return te;
+    } else {
+        memset(&tmap_v, 0, sizeof tmap_v);
+    }
     cudaError_t e = cudaFuncSetAttribute(prep_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)P_SMEM);
@@ -1256,7 +1312,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, recs, st, 2 * sm_count);
+            (int32_t)s0, recs, st, 2 * sm_count, tmap_v);
         if (rec) rec->mark(sp);
         if (piped) {
             e = cudaEventRecord(P->prep_done[par], sp);

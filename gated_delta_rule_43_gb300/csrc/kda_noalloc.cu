@@ -28,7 +28,7 @@ cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t 
                         StatusWord *st, cudaStream_t s);
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
-                            const int32_t *chunk_off, int N, int64_t slots, int H,
+                            const int32_t *chunk_off, int N, int64_t T_tot, int64_t slots, int H,
                             const float *h0, float *S_run, void *o, uint8_t *records,
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec);
@@ -97,6 +97,7 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
         if (!al(p, 16)) return KDA_ERR_INVALID_ARG;
     if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
     if ((total_tokens + kChunk - 1) / kChunk + num_seqs > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
+    if (total_tokens >= ((int64_t)1 << 31)) return KDA_ERR_INVALID_ARG;   // 32-bit tile coordinates
 
     // Scratch layout inside the fixed array; reject what does not fit.
     const bool tc = dtype == KDA_BF16 && dk == 128 && dv == 128;
@@ -132,7 +133,7 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
             e = launch_plan(cu_seqlens, num_seqs, total_tokens, kChunk, chunk_off, st, s);
             if (e == cudaSuccess)
                 e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
-                                    slots, H, initial_state, S_run, o, ws + rec_off, window, 1,
+                                    total_tokens, slots, H, initial_state, S_run, o, ws + rec_off, window, 1,
                                     st, s, nullptr);
         } else {
             e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,

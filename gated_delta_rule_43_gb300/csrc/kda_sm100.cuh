@@ -85,6 +85,18 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// 3-D tiled tensor load through a tensor map (a __grid_constant__ kernel parameter):
+// the box at coordinates (c0 innermost, c1, c2) lands in shared memory as the map's
+// swizzle lays it out; completion counted on `bar`.  c0 * element size must be a
+// multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_3d(void *dst, const void *tmap, int32_t c0, int32_t c1,
+                                            int32_t c2, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(smem_u32(dst)), "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+        : "memory");
+}
 // pull `bytes` of global memory into L2 without waiting (address and size: multiples of 16)
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");

@@ -104,6 +104,7 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
  *   final_state   [num_seqs, H, dk, dv]  fp32 or NULL; may alias initial_state (in-place update)
  *   o             [total_tokens, H, dv]  dtype; must not alias any input
  *   workspace     >= kda_chunk_fwd_workspace_size(...) bytes, 256-byte aligned
+ * Limits: total_tokens < 2^31 on the tensor-core path (KDA_ERR_INVALID_ARG otherwise).
  * Device-found errors: KDA_ERR_SEQLENS (nothing computed for the offending
  * sequence), KDA_ERR_DECAY_RANGE (outputs of that chunk are not meaningful),
  * KDA_ERR_TIMEOUT.

@@ -81,6 +81,9 @@ constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64
 constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
 constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
+constexpr uint32_t P_ZT = 47104;        // (until pass A) z tile, TMA, [2][64][128 B] swizzled
+constexpr uint32_t P_KT = 63488;        // (until the table pass) k tile, likewise
+constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewise
 constexpr uint32_t P_NS = 1024;         // (solve) fp32 N_ab blocks [6][16][16] over the dead tables
 constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], before N
 constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
@@ -93,6 +96,8 @@ static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K image
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
 static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
+static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
+                  P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
 static_assert(P_NS + 6 * 256 * 4 <= P_BETA && P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
                   P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
               "solve / epilogue staging overlaps live data");
@@ -150,7 +155,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
             int32_t slot0, uint8_t *__restrict__ records, StatusWord *st, int ahead,
-            const __grid_constant__ CUtensorMap tmap_v) {
+            const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+            const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -169,29 +175,35 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_BAR + 16);
     uint64_t *vbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 32);   // the V tile's TMA
+    uint64_t *zbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 40);   // the z tile's TMA
+    uint64_t *kqbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 48);  // the k and q tiles' TMA
+
+    // The z, k and q tiles (64 tokens x 128 channels each) arrive by TMA in the 128-byte
+    // swizzled layout, element (r, c) at sw128_offset(r, c, 64), in shared memory that the
+    // element passes overwrite only after reading them.
+    if (tid == 0) {
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(vbar, 1);
+        mbar_init(zbar, 1);
+        mbar_init(kqbar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(zbar, 2 * 8192);
+        tma_load_3d(sm + P_ZT, &tmap_z, 0, h, (int32_t)t0, zbar);
+        tma_load_3d(sm + P_ZT + 8192, &tmap_z, 64, h, (int32_t)t0, zbar);
+        mbar_arrive_expect_tx(kqbar, 4 * 8192);
+        tma_load_3d(sm + P_KT, &tmap_k, 0, h, (int32_t)t0, kqbar);
+        tma_load_3d(sm + P_KT + 8192, &tmap_k, 64, h, (int32_t)t0, kqbar);
+        tma_load_3d(sm + P_QT, &tmap_q, 0, h, (int32_t)t0, kqbar);
+        tma_load_3d(sm + P_QT + 8192, &tmap_q, 64, h, (int32_t)t0, kqbar);
+    }
 
     const int a = warp & 3;                    // this thread's 16-token tile
     const int rl = lane & 15;
     const int r = 16 * a + rl;                 // this thread's row of the chunk
     const bool valid = r < L;
-    const int64_t row_off = ((t0 + r) * H + h) * (int64_t)DK;
-    // All of this thread's global reads (A_log, beta, z, k, q) are issued before any set-up.
     const float alog = A_log[h];
     const float beta_v = tid < L ? __bfloat162float(beta[(t0 + min(tid, C - 1)) * H + h]) : 0.f;
-    uint4 zraw[NU], kraw[NU], qraw[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-        zraw[u] = valid ? *reinterpret_cast<const uint4 *>(z + row_off + c) : zero;
-    }
-#pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
-        const uint4 zero = make_uint4(0, 0, 0, 0);
-        kraw[u] = valid ? *reinterpret_cast<const uint4 *>(k + row_off + c) : zero;
-        qraw[u] = valid ? *reinterpret_cast<const uint4 *>(q + row_off + c) : zero;
-    }
     // The CTA `ahead` blocks later in launch order starts about one wave after this one:
     // pull its q, k, z, v rows into L2 now (thread = (tensor, row), two 128-byte lines).
     {
@@ -211,11 +223,13 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     }
     const float expA = expf(alog);
     if (tid < C) BETA[tid] = beta_v;
-    if (tid == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
-        mbar_init(vbar, 1);
-        fence_mbar_init();
+    __syncthreads();                           // the barriers' initialisation is visible
+    bool ok = mbar_wait(zbar, 0);
+    uint4 zraw[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
+        zraw[u] = *reinterpret_cast<const uint4 *>(sm + P_ZT + sw128_offset(r, c, 64));
     }
 
     // ---- (A) gate into the fp32 G scratch (row-wise, 16-byte stores), then the in-tile
@@ -251,11 +265,20 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
     }
     __syncthreads();
-    // this thread's G values, read before pass B reuses the scratch
+    // this thread's G values and k, q chunks, read before pass B reuses their space
     float trun[NU][8];
 #pragma unroll
     for (int u = 0; u < NU; ++u)
         ld8(GS + r * GLD + 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4)), trun[u]);
+    ok = mbar_wait(kqbar, 0) && ok;
+    uint4 kraw[NU], qraw[NU];
+#pragma unroll
+    for (int u = 0; u < NU; ++u) {
+        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
+        const uint4 zero = make_uint4(0, 0, 0, 0);
+        kraw[u] = valid ? *reinterpret_cast<const uint4 *>(sm + P_KT + sw128_offset(r, c, 64)) : zero;
+        qraw[u] = valid ? *reinterpret_cast<const uint4 *>(sm + P_QT + sw128_offset(r, c, 64)) : zero;
+    }
     if (warp == PREP_THREADS / 32 - 1) {   // idle during the table pass
         tmem_alloc(tslot, 256);
         tmem_relinquish();
@@ -347,7 +370,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
         bulk_commit();
     }
-    bool ok = mbar_wait(&bar[0], 0);
+    ok = mbar_wait(&bar[0], 0) && ok;
     tc_fence_after();
     // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region: the V half arrives
     //          by TMA (two 64-channel boxes of 64 tokens, 128-byte swizzle, which is the
@@ -1253,11 +1276,17 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec) {
     using namespace tc;
-    CUtensorMap tmap_v;
+    CUtensorMap tmap_q, tmap_k, tmap_z, tmap_v;
     if (T_tot > 0) {
-        cudaError_t te = tmap_thd(&tmap_v, v, T_tot, H);
+        cudaError_t te = tmap_thd(&tmap_q, q, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_k, k, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_z, z, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_v, v, T_tot, H);
         if (te != cudaSuccess) return te;
     } else {
+        memset(&tmap_q, 0, sizeof tmap_q);
+        memset(&tmap_k, 0, sizeof tmap_k);
+        memset(&tmap_z, 0, sizeof tmap_z);
         memset(&tmap_v, 0, sizeof tmap_v);
     }
     cudaError_t e = cudaFuncSetAttribute(prep_kernel,
@@ -1312,7 +1341,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, recs, st, 2 * sm_count, tmap_v);
+            (int32_t)s0, recs, st, 2 * sm_count, tmap_q, tmap_k, tmap_z, tmap_v);
         if (rec) rec->mark(sp);
         if (piped) {
             e = cudaEventRecord(P->prep_done[par], sp);

@@ -19,44 +19,49 @@
 namespace kda {
 
 constexpr int kDecodeThreads = 256;
+constexpr int kDecodeSplit128 = 64;   // value columns per CTA at dv = 128
 
-template <int DK, int DV, typename T>
+// One CTA per (n, h, block of DVC value columns); DV / DVC CTAs share one (n, h).
+template <int DK, int DV, int DVC, typename T>
 __global__ void __launch_bounds__(kDecodeThreads)
 decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    const T *__restrict__ z, const T *__restrict__ beta,
                    const float *__restrict__ A_log, float *__restrict__ state,
                    T *__restrict__ o, int H, const int32_t *__restrict__ slot_idx, int P,
                    StatusWord *st) {
-    constexpr int TPR = DV / 4;                 // threads covering one row (float4 each)
+    constexpr int TPR = DVC / 4;                // threads covering one row (float4 each)
     constexpr int RPP = kDecodeThreads / TPR;   // rows covered per pass
     constexpr int R = DK / RPP;                 // rows per thread
-    static_assert(DV % 4 == 0 && kDecodeThreads % TPR == 0 && DK % RPP == 0, "shape");
+    constexpr int NCB = DV / DVC;
+    static_assert(DVC % 4 == 0 && DV % DVC == 0 && kDecodeThreads % TPR == 0 && DK % RPP == 0,
+                  "shape");
 
     __shared__ float s_k[DK], s_q[DK], s_alpha[DK];
-    __shared__ float s_v[DV], s_u[DV];
-    __shared__ __align__(16) float s_pa[RPP][DV];
-    __shared__ __align__(16) float s_pb[RPP][DV];
+    __shared__ float s_v[DVC], s_u[DVC];
+    __shared__ __align__(16) float s_pa[RPP][DVC];
+    __shared__ __align__(16) float s_pb[RPP][DVC];
     __shared__ float s_qk, s_beta;
 
-    const int nh = blockIdx.x;
+    const int nh = blockIdx.x / NCB;
+    const int j0 = (blockIdx.x % NCB) * DVC;
     const int h = nh % H;
     const int n = nh / H;
     const int tid = threadIdx.x;
     const int64_t kb = (int64_t)nh * DK;
-    const int64_t vb = (int64_t)nh * DV;
+    const int64_t vb = (int64_t)nh * DV + j0;
     const int slot = slot_idx ? slot_idx[n] : n;
     if (slot < 0 || slot >= P) {
-        if (tid == 0 && h == 0) report(st, KDA_ERR_INVALID_ARG, n, 20);
+        if (tid == 0 && h == 0 && j0 == 0) report(st, KDA_ERR_INVALID_ARG, n, 20);
         return;
     }
 
     // Issue the state loads first: they are the bulk of the traffic.
     const int c4 = tid % TPR;
     const int rg = tid / TPR;
-    float4 *S4 = reinterpret_cast<float4 *>(state + ((int64_t)slot * H + h) * DK * DV);
+    float4 *S4 = reinterpret_cast<float4 *>(state + ((int64_t)slot * H + h) * DK * DV + j0);
     float4 s[R];
 #pragma unroll
-    for (int p = 0; p < R; ++p) s[p] = __ldcs(S4 + (int64_t)(rg + p * RPP) * TPR + c4);
+    for (int p = 0; p < R; ++p) s[p] = __ldcs(S4 + (int64_t)(rg + p * RPP) * (DV / 4) + c4);
 
     const float expA = expf(A_log[h]);
     for (int i = tid; i < DK; i += kDecodeThreads) {
@@ -64,7 +69,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         s_k[i] = to_f(k[kb + i]);
         s_q[i] = to_f(q[kb + i]);
     }
-    for (int j = tid; j < DV; j += kDecodeThreads) s_v[j] = to_f(v[vb + j]);
+    for (int j = tid; j < DVC; j += kDecodeThreads) s_v[j] = to_f(v[vb + j]);
     if (tid == 0) s_beta = to_f(beta[nh]);
     __syncthreads();
     if (tid < 32) {
@@ -87,7 +92,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     *reinterpret_cast<float4 *>(&s_pa[rg][c4 * 4]) = make_float4(pa[0], pa[1], pa[2], pa[3]);
     *reinterpret_cast<float4 *>(&s_pb[rg][c4 * 4]) = make_float4(pb[0], pb[1], pb[2], pb[3]);
     __syncthreads();
-    for (int j = tid; j < DV; j += kDecodeThreads) {
+    for (int j = tid; j < DVC; j += kDecodeThreads) {
         float a = 0.f, b = 0.f;
 #pragma unroll 8
         for (int g = 0; g < RPP; ++g) {
@@ -107,7 +112,7 @@ decode_step_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
         const float kr = s_k[row];
         float4 w = s[p];
         w.x += kr * u0; w.y += kr * u1; w.z += kr * u2; w.w += kr * u3;
-        __stcs(S4 + (int64_t)row * TPR + c4, w);
+        __stcs(S4 + (int64_t)row * (DV / 4) + c4, w);
     }
 }
 
@@ -116,7 +121,11 @@ static cudaError_t launch_decode_t(const void *q, const void *k, const void *v, 
                                    const void *beta, const float *A_log, float *state, void *o,
                                    int N, int H, const int32_t *slot_idx, int P, StatusWord *st,
                                    cudaStream_t stream) {
-    decode_step_kernel<DK, DV, T><<<(unsigned)((int64_t)N * H), kDecodeThreads, 0, stream>>>(
+    // dv = 128 splits into two 64-column CTAs: half the registers per thread, so more CTAs
+    // (and more of the state) in flight per SM
+    constexpr int DVC = DV == 128 ? kDecodeSplit128 : DV;
+    decode_step_kernel<DK, DV, DVC, T>
+        <<<(unsigned)((int64_t)N * H * (DV / DVC)), kDecodeThreads, 0, stream>>>(
         (const T *)q, (const T *)k, (const T *)v, (const T *)z, (const T *)beta, A_log, state,
         (T *)o, H, slot_idx, P, st);
     return cudaGetLastError();

@@ -87,13 +87,13 @@ def prefill_flops(seqlens, H, dk, dv) -> int:
     return sum(seqlens) * H * (6 * dk * dv + 64 * (3 * dk + 2 * dv))
 
 
-def kernel_names(n_events: int, tc_path: bool, has_init: bool) -> list[str]:
+def kernel_names(n_events: int, tc_path: bool) -> list[str]:
     """Names of the kernels one kda_chunk_fwd_profiled call launched, in order (each
     kernel is bracketed by a pair of events recorded on its own stream)."""
     k = n_events // 2
     if not tc_path:
         return ["chunk_fwd_simt_kernel"] * k
-    names = ["plan_chunks_kernel"] + (["state_init_kernel"] if has_init else [])
+    names = ["plan_chunks_kernel"]
     while len(names) < k:
         names += ["prep_kernel", "chain_kernel"]
     return names[:k]
@@ -261,7 +261,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     kda.query_status(ws, stream, raise_on_error=True)
     names = kernel_names(used[0], tc_path=(d["q"].dtype == torch.bfloat16 and dk == 128
-                                            and dv == 128), has_init=d["h0"] is not hT)
+                                            and dv == 128))
     per_kernel = {}
     for i in range(K):
         for j, nm in enumerate(names):

@@ -18,6 +18,9 @@ cudaError_t launch_chunk_simt(int dtype, int dk, int dv, const void *q, const vo
                               cudaStream_t s, EventRec *rec);
 cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
                         StatusWord *st, cudaStream_t s);
+cudaError_t launch_plan_tc(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
+                           StatusWord *st, const float *h0, float *S_run, int H, int64_t dkdv,
+                           int grid, cudaStream_t s);
 size_t tc_record_bytes();
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
@@ -127,15 +130,18 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
 
     cudaStream_t s = (cudaStream_t)stream;
     StatusWord *st = (StatusWord *)workspace;
-    cudaError_t e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
-    if (e != cudaSuccess) return KDA_ERR_CUDA;
-    if (num_seqs == 0) return KDA_OK;
-    if (use_tc(dtype, dk, dv)) {
+    cudaError_t e = cudaSuccess;
+    if (num_seqs > 0 && use_tc(dtype, dk, dv)) {
+        // the plan kernel clears the status word and gives chunk-less sequences their
+        // final state; the chain kernels read the initial state themselves
         uint8_t *ws = (uint8_t *)workspace;
         int32_t *chunk_off = (int32_t *)(ws + L.plan_off);
         float *S_run = final_state ? final_state : (float *)(ws + L.state_off);
+        const int64_t nh = (int64_t)num_seqs * H;
         if (rec) rec->mark(s);
-        e = launch_plan(cu_seqlens, num_seqs, total_tokens, kTcChunk, chunk_off, st, s);
+        e = launch_plan_tc(cu_seqlens, num_seqs, total_tokens, kTcChunk, chunk_off, st,
+                           initial_state, S_run, H, (int64_t)dk * dv, (int)(nh < 256 ? nh : 256),
+                           s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
         if (rec) rec->mark(s);
         e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
@@ -144,6 +150,9 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
                             rec);
         return cuda_status(e);
     }
+    e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
+    if (e != cudaSuccess) return KDA_ERR_CUDA;
+    if (num_seqs == 0) return KDA_OK;
     e = launch_chunk_simt(dtype, dk, dv, q, k, v, z, beta, A_log, cu_seqlens, num_seqs,
                           total_tokens, H, initial_state, final_state, o, st, s, rec);
     return cuda_status(e);

@@ -712,7 +712,8 @@ __device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float 
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
-             float *__restrict__ state, __nv_bfloat16 *__restrict__ o, StatusWord *st) {
+             const float *h0, float *__restrict__ state, __nv_bfloat16 *__restrict__ o,
+             StatusWord *st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -766,11 +767,16 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         const int64_t eos = cu[n + 1];
         const int j0 = blk * DVB;
         float S[DVB];
-        float *srow = state + (((int64_t)n * H + h) * DK + i) * DV + j0;
+        const int64_t soff = (((int64_t)n * H + h) * DK + i) * DV + j0;
+        float *srow = state + soff;
+        // the sequence's first chunk starts from h0 (zeros when absent), later windows from
+        // the running state
+        const float *s_in = c_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
         if (warp < 4) {
 #pragma unroll
             for (int j4 = 0; j4 < DVB / 4; ++j4) {
-                const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
+                const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
             }
             store_row_sw64(sm + C_S, i, S);
@@ -982,7 +988,8 @@ __device__ __forceinline__ void store_row_sw128(uint8_t *img, int r, int j0, uin
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
-             float *__restrict__ state, __nv_bfloat16 *__restrict__ o, StatusWord *st) {
+             const float *h0, float *__restrict__ state, __nv_bfloat16 *__restrict__ o,
+             StatusWord *st) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1032,10 +1039,15 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         const int64_t bos = cu[n];
         const int64_t eos = cu[n + 1];
         float S[32];
-        float *srow = state + (((int64_t)n * H + h) * DK + i) * DV + j0;
+        const int64_t soff = (((int64_t)n * H + h) * DK + i) * DV + j0;
+        float *srow = state + soff;
+        // the sequence's first chunk starts from h0 (zeros when absent), later windows from
+        // the running state
+        const float *s_in = c_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
 #pragma unroll
         for (int j4 = 0; j4 < 8; ++j4) {
-            const float4 x = reinterpret_cast<const float4 *>(srow)[j4];
+            const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
         }
         store_row_sw128(sm + C_S, i, j0, DK, S);
@@ -1180,15 +1192,6 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
 
 }  // namespace c128
 
-// Copy (or zero) the initial state into the running-state buffer.
-__global__ void state_init_kernel(const float *__restrict__ h0, float *__restrict__ S,
-                                  int64_t n4) {
-    for (int64_t e = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; e < n4;
-         e += (int64_t)gridDim.x * blockDim.x)
-        reinterpret_cast<float4 *>(S)[e] =
-            h0 ? reinterpret_cast<const float4 *>(h0)[e] : make_float4(0.f, 0.f, 0.f, 0.f);
-}
-
 }  // namespace tc
 
 size_t tc_record_bytes() { return tc::REC_BYTES; }
@@ -1303,13 +1306,6 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
     e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const int64_t n4 = (int64_t)N * H * DK * DV / 4;
-    if (h0 != S_run) {
-        const int64_t blocks = std::min<int64_t>((n4 + 255) / 256, (int64_t)sm_count * 16);
-        if (rec) rec->mark(s);
-        state_init_kernel<<<(unsigned)blocks, 256, 0, s>>>(h0, S_run, n4);
-        if (rec) rec->mark(s);
-    }
     const bool piped = nbuf == 2 && slots > window;
     Pipe *P = nullptr;
     std::unique_lock<std::mutex> lock(g_pipe_mutex, std::defer_lock);
@@ -1359,12 +1355,12 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         if (items32 <= (piped ? (int64_t)sm_count / 2 : 2 * (int64_t)sm_count)) {
             const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
             c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, sc>>>(
-                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, S_run,
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,
                 (__nv_bfloat16 *)o, st);
         } else {
             const int64_t grid = std::min<int64_t>(seqs * H, sm_count);
             c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, sc>>>(
-                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, S_run,
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,
                 (__nv_bfloat16 *)o, st);
         }
         if (rec) rec->mark(sc);

@@ -9,15 +9,40 @@
 
 namespace kda {
 
-// chunk_off[n] = sum over m < n of ceil(len_m / C), for n = 0..N (one CTA).
+// chunk_off[n] = sum over m < n of ceil(len_m / C), for n = 0..N (CTA 0).
 // Validates cu_seqlens (0-based, non-decreasing, ending at T_tot); an invalid
-// sequence is recorded as KDA_ERR_SEQLENS and given zero chunks.
+// sequence is recorded as KDA_ERR_SEQLENS and given zero chunks.  With
+// clear_status the grid's single CTA first zeroes the status word (it is the first
+// kernel of a call, so nothing has reported yet).  With S_run != NULL every CTA also
+// gives each sequence that owns no chunk (empty or invalid) its final state: h0's
+// (zeros when h0 is NULL) -- the chunk kernels only write states of sequences they walk.
 __global__ void __launch_bounds__(1024)
 plan_chunks_kernel(const int32_t *__restrict__ cu, int N, int64_t T_tot, int C,
-                   int32_t *__restrict__ chunk_off, StatusWord *st) {
+                   int32_t *__restrict__ chunk_off, StatusWord *st, int clear_status,
+                   const float *__restrict__ h0, float *__restrict__ S_run, int H,
+                   int64_t dkdv4) {
+    if (S_run) {   // grid-stride over (sequence, head) pairs of chunk-less sequences
+        for (int64_t nh = blockIdx.x; nh < (int64_t)N * H; nh += gridDim.x) {
+            const int n = (int)(nh / H);
+            const int64_t b = cu[n], e = cu[n + 1];
+            if (b < e && b >= 0 && e <= T_tot) continue;
+            float4 *dst = reinterpret_cast<float4 *>(S_run) + nh * dkdv4;
+            const float4 *src = h0 ? reinterpret_cast<const float4 *>(h0) + nh * dkdv4 : nullptr;
+            for (int64_t i = threadIdx.x; i < dkdv4; i += blockDim.x)
+                dst[i] = src ? src[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    if (blockIdx.x != 0) return;
     __shared__ int32_t s_warp[32];
     __shared__ int32_t s_carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    if (clear_status && tid == 0) {
+        st->code = 0u;
+        st->site = 0u;
+        st->info = 0ull;
+        __threadfence();
+    }
+    __syncthreads();
     if (tid == 0) {
         s_carry = 0;
         if (cu[0] != 0 || (int64_t)cu[N] != T_tot) report(st, KDA_ERR_SEQLENS, N, 1);
@@ -111,7 +136,19 @@ __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restr
 
 cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
                         StatusWord *st, cudaStream_t s) {
-    plan_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T_tot, C, chunk_off, st);
+    plan_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 0, nullptr, nullptr,
+                                          0, 0);
+    return cudaGetLastError();
+}
+
+// The plan of the tensor-core path: also clears the status word and writes the final
+// states of chunk-less sequences into S_run (skipped when S_run is h0, an in-place update).
+cudaError_t launch_plan_tc(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
+                           StatusWord *st, const float *h0, float *S_run, int H, int64_t dkdv,
+                           int grid, cudaStream_t s) {
+    const bool init = S_run != h0;
+    plan_chunks_kernel<<<init ? grid : 1, 1024, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 1, h0,
+                                                       init ? S_run : nullptr, H, dkdv / 4);
     return cudaGetLastError();
 }
 

@@ -24,8 +24,9 @@
 #include "kda_common.cuh"
 
 namespace kda {
-cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
-                        StatusWord *st, cudaStream_t s);
+cudaError_t launch_plan_tc(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
+                           StatusWord *st, const float *h0, float *S_run, int H, int64_t dkdv,
+                           int grid, cudaStream_t s);
 cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const void *z,
                             const void *beta, const float *A_log, const int32_t *cu,
                             const int32_t *chunk_off, int N, int64_t T_tot, int64_t slots, int H,
@@ -130,7 +131,10 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
         if (tc) {
             int32_t *chunk_off = (int32_t *)(ws + plan_off);
             float *S_run = final_state ? final_state : (float *)(ws + state_off);
-            e = launch_plan(cu_seqlens, num_seqs, total_tokens, kChunk, chunk_off, st, s);
+            const int64_t nh = (int64_t)num_seqs * H;
+            e = launch_plan_tc(cu_seqlens, num_seqs, total_tokens, kChunk, chunk_off, st,
+                               initial_state, S_run, H, (int64_t)dk * dv,
+                               (int)(nh < 256 ? nh : 256), s);
             if (e == cudaSuccess)
                 e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
                                     total_tokens, slots, H, initial_state, S_run, o, ws + rec_off, window, 1,

@@ -123,9 +123,9 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
  * (before) and events[2j+1] (after), both recorded on the stream that kernel is
  * launched on, for as many kernels as fit, and writes the number of events
  * recorded to *n_recorded (host pointer).  The kernels of one call on the
- * tensor-core path are, in launch order: the chunk plan,
- * the running-state initialisation (absent when initial_state aliases
- * final_state), then one (prep, chain) pair per window of chunk records; on
+ * tensor-core path are, in launch order: the chunk plan (which also clears the
+ * status word and writes the final state of sequences that own no chunk), then
+ * one (prep, chain) pair per window of chunk records; on
  * the CUDA-core path, one chunked kernel.  Used by the benchmark to time the
  * dominant kernel on its own launch stream.
  */

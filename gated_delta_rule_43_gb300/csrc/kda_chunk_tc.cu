@@ -668,24 +668,25 @@ namespace c32 {
 
 constexpr int DVB = 32;          // value columns per CTA
 constexpr int NBLK = DV / DVB;
-constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [0; P] U
-constexpr uint32_t B_WQ = 0, B_KT = 32768, B_ZP = 49152, B_U = 65536, B_G = 73728;
-constexpr uint32_t BUF_BYTES = 74752;
+constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x; P] U
+// a record buffer mirrors the record's first 57344 bytes (WQ, KT, P), then this CTA's U
+// block and Gam_C
+constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = 65536;
+constexpr uint32_t BUF_BYTES = 66560;
 constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
 constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
 constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, m3, TMEM slot, abort flag
 constexpr uint32_t C_SMEM = C_BAR + 64 + 1024;
-constexpr uint32_t LOAD_BYTES = 32768 + 16384 + 8192 + 8192 + 512;
-static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0, "chain buffer layout");
+constexpr uint32_t LOAD_BYTES = REC_U + 8192 + 512;
+static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0 && B_P == REC_P && B_KT == REC_KT,
+              "chain buffer layout");
 static_assert(C_S % 1024 == 0 && C_UI % 1024 == 0, "operand image alignment");
 static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int blk,
                                            uint64_t *full) {
     mbar_arrive_expect_tx(full, LOAD_BYTES);
-    bulk_g2s(buf + B_WQ, rec + REC_WQ, 32768, full);
-    bulk_g2s(buf + B_KT, rec + REC_KT, 16384, full);
-    bulk_g2s(buf + B_ZP + 8192, rec + REC_P, 8192, full);
+    bulk_g2s(buf, rec, REC_U, full);   // WQ, KT, P in one copy
     bulk_g2s(buf + B_U, rec + REC_U + blk * 8192, 8192, full);
     bulk_g2s(buf + B_G, rec + REC_G, 512, full);
 }
@@ -706,7 +707,7 @@ __device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float 
 // in order, carrying its block of S in registers (fp32, thread i = row i) and as
 // the bf16 B operand image.  Per chunk, on the critical path:
 //   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
-//   D1 += [0; P] U     ->  S = Diag(Gam_C) S + D2.
+//   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
 // D1 is double-buffered in TMEM so that the output rows of chunk c (D1[64:128])
 // are stored by warps 2-3 while warps 0-1 form U of chunk c+1.
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
@@ -731,11 +732,6 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
         *abort_flag = 0;
         fence_mbar_init();
-    }
-    // zero rows 0..63 of both [0; P] operand images
-    for (int e = tid; e < 2 * 512; e += CHAIN_THREADS) {
-        uint8_t *b = sm + (e / 512) * BUF_BYTES + B_ZP;
-        reinterpret_cast<uint4 *>(b)[e % 512] = make_uint4(0, 0, 0, 0);
     }
     if (warp == 0) {
         tmem_alloc(tslot, 128);
@@ -789,7 +785,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                        &bar[gi & 1]);
 
         // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
-        // (warps 2-3); waits for that chunk's [0; P] U product (barrier m3)
+        // (warps 2-3); waits for that chunk's [x; P] U product (barrier m3)
         auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
             const uint32_t pb = gprev & 1;
             if (!mbar_wait(&bar[4], gprev & 1)) return false;
@@ -845,12 +841,12 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                         acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
                         acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
                     }
-                    // the U image is free once the previous chunk's [0; P] U product is done
+                    // the U image is free once the previous chunk's [x; P] U product is done
                     if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                     store_row_sw64(sm + C_UI, r, acc);
                 }
             } else if (warp < 4) {
-                // previous chunk's outputs, off the critical path; its [0; P] U product was
+                // previous chunk's outputs, off the critical path; its [x; P] U product was
                 // the last reader of the other buffer, which then takes the next chunk
                 if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
                 if (tid == 64 && ok && cs + 1 < c_end)
@@ -882,10 +878,12 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             ok = mbar_wait(&bar[3], gi & 1);
             tc_fence_after();
             if (warp == 4) {
-                // ... then D1[b] += [0; P] U (outputs only), issued by warp 4 behind D2 so
-                // that it runs while S is updated
+                // ... then D1[b] += [x; P] U (outputs only), issued by warp 4 behind D2 so
+                // that it runs while S is updated.  [x; P] reads the 64 rows in front of P
+                // (the tail of KT) as its first half; those rows of D1 hold W S, which the
+                // U epilogue has consumed by then.
                 if (lane == 0 && ok) {
-                    const uint64_t azp = sdesc_sw128(bufa + B_ZP, 16, 1024);
+                    const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
 #pragma unroll
                     for (int s = 0; s < C / 16; ++s)
                         umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024), id_km, 1);

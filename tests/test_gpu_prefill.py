@@ -123,10 +123,11 @@ def test_profiled_entry_pairs_and_stream_order():
     kernels on the library's own streams)."""
     # more than one window of chunk records (1 GiB), so that the double-buffered schedule
     # with its own streams runs
-    d = inputs.make_prefill([20000, 4000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
+    # (the empty sequence in the middle owns no chunk: its final state is its initial one)
+    d = inputs.make_prefill([20000, 0, 4000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
                             h0_sigma=0.1, device=DEV)
     T, H, dk = d["q"].shape
-    N = 2
+    N = 3
     ws_bytes = kda.chunk_fwd_workspace_size(T, N, H, dk, 128, torch.bfloat16)
     side = torch.cuda.Stream()
     side.wait_stream(torch.cuda.current_stream())
@@ -149,5 +150,6 @@ def test_profiled_entry_pairs_and_stream_order():
     assert all(ev[j].elapsed_time(ev[j + 1]) >= 0.0 for j in range(0, used, 2))
     assert not torch.isnan(o_host).any()
     assert torch.equal(o, o2) and torch.equal(hT, hT2)
+    assert torch.equal(hT[1], d["h0"][1])
     e_o, e_s = score_prefill(d, o, hT, None, [0, 17, 31])
     assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"]

@@ -952,11 +952,7 @@ static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
 
 __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, uint64_t *full) {
     mbar_arrive_expect_tx(full, REC_BYTES);
-    bulk_g2s(buf + REC_WQ, rec + REC_WQ, REC_KT - REC_WQ, full);
-    bulk_g2s(buf + REC_KT, rec + REC_KT, REC_P - REC_KT, full);
-    bulk_g2s(buf + REC_P, rec + REC_P, REC_U - REC_P, full);
-    bulk_g2s(buf + REC_U, rec + REC_U, REC_G - REC_U, full);
-    bulk_g2s(buf + REC_G, rec + REC_G, REC_BYTES - REC_G, full);
+    bulk_g2s(buf, rec, REC_BYTES, full);   // the whole record, one copy
 }
 
 // 32 fp32 values -> four 16-byte chunks of row r, columns j0.., of a 128B-swizzled

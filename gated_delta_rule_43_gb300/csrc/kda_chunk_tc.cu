@@ -60,9 +60,8 @@ constexpr uint32_t REC_BYTES = 90624;
 constexpr int PREP_THREADS = 256;
 constexpr int PREP_WARPS = PREP_THREADS / 32;
 constexpr int NU = 32 / PREP_WARPS;     // 8-channel units per thread in the element-wise passes
-constexpr int CHG = 2 * NU;             // 8-channel chunks per warp (per half-warp: NU)
 constexpr int SOLVE_W = (384 + 128 + PREP_THREADS - 1) / PREP_THREADS;   // solve tasks per thread
-static_assert(PREP_WARPS == 8 || PREP_WARPS == 16, "prep kernel runs 8 or 16 warps");
+static_assert(PREP_WARPS == 8 && NU == 4, "row-wise passes map 8 warps x 32 lanes onto 16 rows x 16 chunks, one unit per tile");
 constexpr int LDA = 68;                 // row stride (floats) of the fp32 A and T tiles
 // Shared-memory map of the prep kernel (offsets from a 1024-aligned base).  Two
 // CTAs fit on one SM.  Regions are reused once the A/P products have completed.
@@ -144,11 +143,10 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
     return L > 0;
 }
 
-// One CTA per (chunk slot, head).  Work split for the row-wise element passes:
-// warp w takes 16-token tile a = w & 3 and channel-chunk group w >> 2; lane l
-// takes row 16a + (l & 15); its NU units are 8-channel chunks
-// ch = CHG (w >> 2) + 2u + (l >> 4), u = 0..NU-1.  The in-tile cumulative sums
-// run down the columns of a shared-memory scratch, one (tile, channel) per thread.
+// One CTA per (chunk slot, head).  Work split for the row-wise element passes: lane l of
+// warp w takes the 8-channel chunk ch = 2w + (l >> 4) of rows 16u + (l & 15), one in each
+// 16-token tile u = 0..3.  The in-tile cumulative sums run down the columns of a
+// shared-memory scratch, one (tile, channel) per thread.
 __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
@@ -198,10 +196,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tma_load_3d(sm + P_QT + 8192, &tmap_q, 64, h, (int32_t)t0, kqbar);
     }
 
-    const int a = warp & 3;                    // this thread's 16-token tile
+    // Row-wise element passes: thread (row-in-tile rl, 8-channel chunk ch) owns unit u =
+    // row 16u + rl of tile u, u = 0..3, so that every thread writes the same number of
+    // column-scaled key images (tile a's rows appear in images a..3).
     const int rl = lane & 15;
-    const int r = 16 * a + rl;                 // this thread's row of the chunk
-    const bool valid = r < L;
+    const int ch = 2 * warp + (lane >> 4);
+    const int c = 8 * ch;
     const float alog = A_log[h];
     const float beta_v = tid < L ? __bfloat162float(beta[(t0 + min(tid, C - 1)) * H + h]) : 0.f;
     // The CTA `ahead` blocks later in launch order starts about one wave after this one:
@@ -227,10 +227,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     bool ok = mbar_wait(zbar, 0);
     uint4 zraw[NU];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
-        zraw[u] = *reinterpret_cast<const uint4 *>(sm + P_ZT + sw128_offset(r, c, 64));
-    }
+    for (int u = 0; u < NU; ++u)
+        zraw[u] = *reinterpret_cast<const uint4 *>(sm + P_ZT + sw128_offset(16 * u + rl, c, 64));
 
     // ---- (A) gate into the fp32 G scratch (row-wise, 16-byte stores), then the in-tile
     //          inclusive cumsums down the columns: thread (tile, channel) walks its 16 rows,
@@ -238,12 +236,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     float *GS = reinterpret_cast<float *>(sm + P_G);
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
+        const int r = 16 * u + rl;
         float zz[8];
         unpack8(zraw[u], zz);
 #pragma unroll
         for (int i = 0; i < 8; ++i)   // g = -5 Sigmoid(e^A z), fast exponential and divide
-            zz[i] = valid ? __fdividef(kGMin, 1.0f + __expf(-expA * zz[i])) : 0.f;
+            zz[i] = r < L ? __fdividef(kGMin, 1.0f + __expf(-expA * zz[i])) : 0.f;
         float4 *dst = reinterpret_cast<float4 *>(GS + r * GLD + c);
         dst[0] = make_float4(zz[0], zz[1], zz[2], zz[3]);
         dst[1] = make_float4(zz[4], zz[5], zz[6], zz[7]);
@@ -268,16 +266,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // this thread's G values and k, q chunks, read before pass B reuses their space
     float trun[NU][8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u)
-        ld8(GS + r * GLD + 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4)), trun[u]);
+    for (int u = 0; u < NU; ++u) ld8(GS + (16 * u + rl) * GLD + c, trun[u]);
     ok = mbar_wait(kqbar, 0) && ok;
     uint4 kraw[NU], qraw[NU];
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
+        const int r = 16 * u + rl;
         const uint4 zero = make_uint4(0, 0, 0, 0);
-        kraw[u] = valid ? *reinterpret_cast<const uint4 *>(sm + P_KT + sw128_offset(r, c, 64)) : zero;
-        qraw[u] = valid ? *reinterpret_cast<const uint4 *>(sm + P_QT + sw128_offset(r, c, 64)) : zero;
+        kraw[u] = r < L ? *reinterpret_cast<const uint4 *>(sm + P_KT + sw128_offset(r, c, 64)) : zero;
+        qraw[u] = r < L ? *reinterpret_cast<const uint4 *>(sm + P_QT + sw128_offset(r, c, 64)) : zero;
     }
     if (warp == PREP_THREADS / 32 - 1) {   // idle during the table pass
         tmem_alloc(tslot, 256);
@@ -310,8 +307,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     uint4 kgam[NU];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
-        const int ch = CHG * (warp >> 2) + 2 * u + (lane >> 4);
-        const int c = 8 * ch;
+        const int a = u, r = 16 * u + rl;   // this unit's tile and row of the chunk
         float kk[8], qq[8], er[8], ktf[8];
         unpack8(kraw[u], kk);
         unpack8(qraw[u], qq);
@@ -381,10 +377,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tma_load_3d(sm + P_KGV + 3 * 8192, &tmap_v, 64, h, (int32_t)t0, vbar);
     }
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {
-        const int c = 8 * (CHG * (warp >> 2) + 2 * u + (lane >> 4));
-        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(r, c, 64)) = kgam[u];
-    }
+    for (int u = 0; u < NU; ++u)
+        *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(16 * u + rl, c, 64)) = kgam[u];
     // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
     // warp w reads its own lane quarter t = w & 3 (rows 32t.. of D_t: 16 Kr rows, then
     // 16 Qr rows), column blocks m = 2 (w >> 2) and 2 (w >> 2) + 1 of D_t

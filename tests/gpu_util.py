@@ -60,18 +60,43 @@ def oracle_prefill(d, seqs=None, heads=None, o_cmp=None):
                        o_cmp=o_cmp), tok, hsel
 
 
+# the last score_prefill call's worst per-(sequence, head) relative L2 errors (o, state)
+LAST_WORST = {"o": 0.0, "state": 0.0}
+
+
+def _rel(x, ref):
+    den = float(np.linalg.norm(ref))
+    return float(np.linalg.norm(x - ref)) / den if den > 0 else float(np.linalg.norm(x))
+
+
 def score_prefill(d, o, hT, seqs=None, heads=None):
-    """(rel-L2 of o, rel-L2 of the final state) against the oracle on the selected slice."""
+    """(rel-L2 of o, rel-L2 of the final state) against the oracle on the selected slice,
+    over the whole slice; the worst per-(sequence, head) values go to LAST_WORST."""
     ref, tok, hsel = oracle_prefill(d, seqs, heads)
     dev = o.device
     o_sel = o.index_select(0, torch.as_tensor(tok, device=dev, dtype=torch.long)).index_select(
         1, torch.as_tensor(hsel, device=dev, dtype=torch.long))
-    e_o = rel_l2(to_f64(o_sel), ref["o"])
-    e_s = None
+    o64 = to_f64(o_sel)
+    e_o = rel_l2(o64, ref["o"])
+    cu = d["cu_seqlens"].cpu().numpy().astype(np.int64)
+    N = len(cu) - 1
+    seqs = list(range(N)) if seqs is None else list(seqs)
+    lens = [int(cu[n + 1] - cu[n]) for n in seqs]
+    bounds = np.concatenate([[0], np.cumsum(lens)])
+    worst_o = 0.0
+    for i in range(len(seqs)):
+        for j in range(len(hsel)):
+            a, b = bounds[i], bounds[i + 1]
+            if b > a:
+                worst_o = max(worst_o, _rel(o64[a:b, j], ref["o"][a:b, j]))
+    e_s, worst_s = None, 0.0
     if hT is not None:
-        N = d["cu_seqlens"].numel() - 1
-        seqs = list(range(N)) if seqs is None else list(seqs)
         s_sel = hT.index_select(0, torch.as_tensor(seqs, device=dev, dtype=torch.long))
         s_sel = s_sel.index_select(1, torch.as_tensor(hsel, device=dev, dtype=torch.long))
-        e_s = rel_l2(to_f64(s_sel), ref["state"])
+        s64 = to_f64(s_sel)
+        e_s = rel_l2(s64, ref["state"])
+        for i in range(len(seqs)):
+            for j in range(len(hsel)):
+                worst_s = max(worst_s, _rel(s64[i, j], ref["state"][i, j]))
+    LAST_WORST["o"], LAST_WORST["state"] = worst_o, worst_s
     return e_o, e_s

@@ -3,20 +3,27 @@ import pytest
 import torch
 
 from gated_delta_rule_43_gb300 import inputs, kda
-from tests.gpu_util import TOL, gpu_prefill, rel_l2, score_prefill, to_f64
+from tests.gpu_util import LAST_WORST, TOL, gpu_prefill, rel_l2, score_prefill, to_f64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
 def _run_and_score(d, dtype, seqs=None, heads=None, final=True):
+    """Whole-tensor rel-L2 within the tolerance; the worst single (sequence, head) within
+    three times it (a short sequence's few outputs are a noisier ratio)."""
     o, hT = gpu_prefill(d, final=final)
     torch.cuda.synchronize()
     e_o, e_s = score_prefill(d, o, hT, seqs, heads)
     tol = TOL[dtype]
+    w = dict(LAST_WORST)
     assert e_o <= tol, f"o rel-L2 {e_o:.3e} > {tol}"
+    assert w["o"] <= 3 * tol, f"worst per-(sequence, head) o rel-L2 {w['o']:.3e}"
     if final:
         assert e_s <= tol, f"state rel-L2 {e_s:.3e} > {tol}"
+        assert w["state"] <= 3 * tol, f"worst per-(sequence, head) state rel-L2 {w['state']:.3e}"
+    print(f"rel-L2 o {e_o:.3e} state {e_s} worst per (seq, head): o {w['o']:.3e} "
+          f"state {w['state']:.3e}")
     return e_o, e_s
 
 

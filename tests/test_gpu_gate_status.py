@@ -73,3 +73,39 @@ def test_softplus_baseline_gate_and_the_bound(dtype):
     _, Gb_ref, bad_b = orc.gate(host_z, A, cu, tile=16)
     assert bad_b == 0
     assert float(Gb.min()) >= -80.0
+
+
+def test_tensor_core_path_nan_is_reported_and_isolated():
+    """On the tensor-core path (bf16, 128/128): a NaN z in the second sequence is reported
+    with its (token, head), and the first sequence -- whose last chunk's tile loads also
+    bring in the second sequence's rows -- still matches the oracle."""
+    from tests.gpu_util import TOL, rel_l2, to_f64
+    d = inputs.make_prefill([100, 100], H=2, dk=128, dv=128, dtype="bf16", seed=11,
+                            h0_sigma=0.1, device=DEV)
+    d["z"][130, 1, 7] = float("nan")
+    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(200, 2, 2, 128, 128, torch.bfloat16),
+                             DEV)
+    o, hT = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                          d["cu_seqlens"], d["h0"], workspace=ws)
+    code, info = kda.query_status(ws)
+    assert code == kda.KDA_ERR_DECAY_RANGE and info == 130 * 2 + 1
+    # sequence 0 alone through the oracle
+    h = {n: inputs.host_array(d[n][:100]) for n in ("q", "k", "v", "z", "beta")}
+    ref = orc.forward(h["q"], h["k"], h["v"], h["z"], h["beta"],
+                      d["A_log"].cpu().numpy().astype(np.float64), np.array([0, 100]),
+                      d["h0"][:1].cpu().numpy().astype(np.float64))
+    assert rel_l2(to_f64(o[:100]), ref["o"]) <= TOL["bf16"]
+    assert rel_l2(to_f64(hT[:1]), ref["state"]) <= TOL["bf16"]
+
+
+def test_tensor_core_path_bad_cu_seqlens_are_reported():
+    d = inputs.make_prefill([70, 70, 70], H=1, dk=128, dv=128, dtype="bf16", seed=12,
+                            device=DEV)
+    for bad in ([0, 70, 35, 210], [0, 70, 140, 150], [1, 70, 140, 210]):
+        cu = torch.tensor(bad, dtype=torch.int32, device=DEV)
+        with pytest.raises(kda.KdaError) as ei:
+            kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], cu, check=True)
+        assert ei.value.code == kda.KDA_ERR_SEQLENS
+    o, s = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                         d["cu_seqlens"], check=True)
+    assert torch.isfinite(o).all() and torch.isfinite(s).all()

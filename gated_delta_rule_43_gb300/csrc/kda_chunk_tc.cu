@@ -802,10 +802,33 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             return true;
         };
 
+        bool aborted = false;
         for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
             const uint32_t b = gi & 1;
             uint8_t *buf = sm + b * BUF_BYTES;
             const uint32_t bufa = base + b * BUF_BYTES;
+            if (warp == 4) {
+                // D1[b] += [x; P] U (outputs only), issued behind D2 so that it runs while S is
+                // updated; warp 4 joins no per-chunk barrier.  [x; P] reads the 64 rows in
+                // front of P (the tail of KT) as its first half; those rows of D1 hold W S,
+                // which the U epilogue has consumed by then.
+                const bool ok4 = mbar_wait(&bar[3], gi & 1);
+                if (lane == 0) {
+                    if (ok4) {
+                        tc_fence_after();
+                        const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024),
+                                      id_km, 1);
+                        umma_commit(&bar[4]);
+                    } else {
+                        *abort_flag = 1;
+                    }
+                }
+                if (!ok4) { aborted = true; break; }
+                continue;
+            }
             bool ok = mbar_wait(&bar[b], (gi >> 1) & 1);
             if (tid == 0 && ok) {
                 // D1[b] = [W; Q*Gam] S
@@ -839,7 +862,19 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                     store_row_sw64(sm + C_UI, r, acc);
                 }
-            } else if (warp < 4) {
+                fence_proxy_async();
+                tc_fence_before();
+                // the U image is complete: D2 = (K*Gam_C/Gam)^T U (only warps 0-1 wait here)
+                ok = bar_and(1, 64, ok);
+                if (tid == 0 && ok) {
+                    tc_fence_after();
+                    const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
+                    umma_commit(&bar[3]);
+                }
+            } else {
                 // previous chunk's outputs, off the critical path; its [x; P] U product was
                 // the last reader of the other buffer, which then takes the next chunk
                 if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
@@ -855,36 +890,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     bulk_prefetch_l2(r2 + REC_G, REC_BYTES - REC_G);
                 }
             }
-            if (!ok) *abort_flag = 1;
-            fence_proxy_async();
-            tc_fence_before();
-            __syncthreads();
-            if (*abort_flag) break;
-            if (tid == 0) {
-                tc_fence_after();
-                // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
-                const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
-#pragma unroll
-                for (int s = 0; s < C / 16; ++s)
-                    umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
-                umma_commit(&bar[3]);
-            }
-            ok = mbar_wait(&bar[3], gi & 1);
+            // S <- Diag(Gam_C) S + D2 (row i = tid)
+            ok = mbar_wait(&bar[3], gi & 1) && ok;
             tc_fence_after();
-            if (warp == 4) {
-                // ... then D1[b] += [x; P] U (outputs only), issued by warp 4 behind D2 so
-                // that it runs while S is updated.  [x; P] reads the 64 rows in front of P
-                // (the tail of KT) as its first half; those rows of D1 hold W S, which the
-                // U epilogue has consumed by then.
-                if (lane == 0 && ok) {
-                    const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
-#pragma unroll
-                    for (int s = 0; s < C / 16; ++s)
-                        umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024), id_km, 1);
-                    umma_commit(&bar[4]);
-                }
-            } else if (ok) {
-                // S <- Diag(Gam_C) S + D2 (row i = tid)
+            if (ok) {
                 const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
                 float acc[32];
                 tmem_ld32(D2 + lane_base, acc);
@@ -892,15 +901,18 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
 #pragma unroll
                 for (int j = 0; j < DVB; ++j) S[j] = gc * S[j] + acc[j];
                 store_row_sw64(sm + C_S, i, S);
-            } else {
-                *abort_flag = 1;
             }
             fence_proxy_async();
             tc_fence_before();
-            __syncthreads();
-            if (*abort_flag) break;
+            // warps 0-3: S image complete and this chunk's record reads done; the AND makes
+            // the decision to stop the same for all of them
+            if (!bar_and(2, 128, ok && !*abort_flag)) {
+                if (tid == 0) *abort_flag = 1;
+                aborted = true;
+                break;
+            }
         }
-        if (*abort_flag) {
+        if (aborted) {
             if (tid == 0) report(st, KDA_ERR_TIMEOUT, ((int64_t)n * H + h) * NBLK + blk, 11);
         } else {
             tc_fence_after();

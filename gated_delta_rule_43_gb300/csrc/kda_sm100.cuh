@@ -121,6 +121,21 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// Named barrier `id` over `n` threads (a multiple of 32) that also ANDs a predicate
+// across them: every participant gets the same answer.
+__device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(n)
+        : "memory");
+    return r != 0;
+}
+
 // ---------------------------------------------------------------- TMEM
 // executed by one whole warp; the TMEM base address is written to *dst
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {

@@ -11,8 +11,9 @@
 //   O  = (Q*Gam) S + P U,    P = lower_incl( [(q_r*Gam_r).(k_j/Gam_j)] )
 //   S <- Diag(Gam_C) S + (K*Gam_C/Gam)^T U
 // Everything but the last three products is independent of S, so it runs in
-// a parallel "prep" kernel over all (chunk, head) pairs; a "chain" kernel per
-// (sequence, head, 32-column block of dv) then walks the chunks in order.
+// a parallel "prep" kernel over all (chunk, head) pairs; a "chain" kernel then walks
+// the chunks in order, one CTA per (sequence, head, 32-column block of dv) or, when
+// there are many sequences, per (sequence, head) with all 128 columns.
 //
 // Numerics (the page's point about 16-token tiles): exp(G_r - G_j) is never
 // formed from a chunk-global exp(-G).  For row r in 16-token tile a, with

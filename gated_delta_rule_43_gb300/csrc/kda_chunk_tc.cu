@@ -353,19 +353,24 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- A and P: D = [Kr; Qr] x [Kc_0; Kc_1; Kc_2; Kc_3]^T (M = 128, N = 160, K = dk);
     //      tile a's block D_a = [Kr; Qr] x Kc_a^T sits in columns 8 a (a + 1) .. + 16 (a + 1)
-    if (tid == 0) {
+    if (warp == 0) {
         const uint32_t idesc = idesc_bf16(128, KC_ROWS, false, false);
         const uint64_t ad = sdesc_sw128(base + P_KRQR, 16, 1024);
         const uint64_t bd = sdesc_sw128(base + P_KC, 16, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int s = 0; s < DK / 16; ++s)
-            umma_bf16(tmem, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
-                      desc_add(bd, (s >> 2) * KC_ROWS * 128 + (s & 3) * 32), idesc, s > 0);
-        umma_commit(&bar[0]);
-        // Q*Gam (staged in pass B) -> rows 64..127 of the record's WQ image, both K halves
-        bulk_s2g(rec + REC_WQ + 8192, sm + P_QST, 8192);
-        bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
-        bulk_commit();
+            for (int s = 0; s < DK / 16; ++s)
+                umma_bf16(tmem, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                          desc_add(bd, (s >> 2) * KC_ROWS * 128 + (s & 3) * 32), idesc, s > 0);
+            umma_commit(&bar[0]);
+        }
+        __syncwarp();
+        if (lane == 0) {
+            // Q*Gam (staged in pass B) -> rows 64..127 of the record's WQ image, both K halves
+            bulk_s2g(rec + REC_WQ + 8192, sm + P_QST, 8192);
+            bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
+            bulk_commit();
+        }
     }
     ok = mbar_wait(&bar[0], 0) && ok;
     tc_fence_after();
@@ -574,16 +579,19 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     __syncthreads();
 
     // ---- (E) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
-    if (tid == 0) {
+    if (warp == 0) {
         ok = mbar_wait(vbar, 0) && ok;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, 256, false, true);
         const uint64_t ad = sdesc_sw128(base + P_TB, 16, 1024);
         const uint64_t bd = sdesc_sw128(base + P_KGV, 64 * 128, 1024);
+        if (elect_one()) {
 #pragma unroll
-        for (int s = 0; s < C / 16; ++s)
-            umma_bf16(tmem, desc_add(ad, s * 32), desc_add(bd, s * 2048), idesc, s > 0);
-        umma_commit(&bar[1]);
+            for (int s = 0; s < C / 16; ++s)
+                umma_bf16(tmem, desc_add(ad, s * 32), desc_add(bd, s * 2048), idesc, s > 0);
+            umma_commit(&bar[1]);
+        }
+        __syncwarp();
     }
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
@@ -813,33 +821,38 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 // updated; warp 4 joins no per-chunk barrier.  [x; P] reads the 64 rows in
                 // front of P (the tail of KT) as its first half; those rows of D1 hold W S,
                 // which the U epilogue has consumed by then.
-                const bool ok4 = mbar_wait(&bar[3], gi & 1);
-                if (lane == 0) {
-                    if (ok4) {
-                        tc_fence_after();
-                        const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
+                const bool ok4 = __all_sync(0xffffffffu, mbar_wait(&bar[3], gi & 1));
+                if (ok4) {
+                    tc_fence_after();
+                    const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
+                    if (elect_one()) {
 #pragma unroll
                         for (int s = 0; s < C / 16; ++s)
                             umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024),
                                       id_km, 1);
                         umma_commit(&bar[4]);
-                    } else {
-                        *abort_flag = 1;
                     }
+                    __syncwarp();
+                } else {
+                    if (lane == 0) *abort_flag = 1;
+                    aborted = true;
+                    break;
                 }
-                if (!ok4) { aborted = true; break; }
                 continue;
             }
             bool ok = mbar_wait(&bar[b], (gi >> 1) & 1);
-            if (tid == 0 && ok) {
+            if (warp == 0 && __all_sync(0xffffffffu, ok)) {
                 // D1[b] = [W; Q*Gam] S
                 tc_fence_after();
                 const uint64_t ad = sdesc_sw128(bufa + B_WQ, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < DK / 16; ++s)
-                    umma_bf16(tmem + 32 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
-                              desc_add(bd_s, s * 1024), id_km, s > 0);
-                umma_commit(&bar[2]);
+                    for (int s = 0; s < DK / 16; ++s)
+                        umma_bf16(tmem + 32 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                                  desc_add(bd_s, s * 1024), id_km, s > 0);
+                    umma_commit(&bar[2]);
+                }
+                __syncwarp();
             }
             if (warp < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
@@ -867,13 +880,16 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 tc_fence_before();
                 // the U image is complete: D2 = (K*Gam_C/Gam)^T U (only warps 0-1 wait here)
                 ok = bar_and(1, 64, ok);
-                if (tid == 0 && ok) {
+                if (warp == 0 && ok) {
                     tc_fence_after();
                     const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
+                    if (elect_one()) {
 #pragma unroll
-                    for (int s = 0; s < C / 16; ++s)
-                        umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
-                    umma_commit(&bar[3]);
+                        for (int s = 0; s < C / 16; ++s)
+                            umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
+                        umma_commit(&bar[3]);
+                    }
+                    __syncwarp();
                 }
             } else {
                 // previous chunk's outputs, off the critical path; its [x; P] U product was
@@ -1087,15 +1103,18 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             uint8_t *buf = sm + buf_off(b);
             const uint32_t bufa = base + buf_off(b);
             bool ok = mbar_wait(&bar[b], (gi >> 1) & 1);
-            if (tid == 0 && ok) {
+            if (warp == 0 && __all_sync(0xffffffffu, ok)) {
                 // D1[b] = [W; Q*Gam] S
                 tc_fence_after();
                 const uint64_t ad = sdesc_sw128(bufa + REC_WQ, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < DK / 16; ++s)
-                    umma_bf16(tmem + 128 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
-                              desc_add(bd_s, s * 2048), id_km, s > 0);
-                umma_commit(&bar[2]);
+                    for (int s = 0; s < DK / 16; ++s)
+                        umma_bf16(tmem + 128 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                                  desc_add(bd_s, s * 2048), id_km, s > 0);
+                    umma_commit(&bar[2]);
+                }
+                __syncwarp();
             }
             if (q4 < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
@@ -1135,20 +1154,23 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             tc_fence_before();
             __syncthreads();
             if (*abort_flag) break;
-            if (tid == 0) {
+            if (warp == 0) {
                 tc_fence_after();
                 // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
                 const uint64_t akt = sdesc_sw128(bufa + REC_KT, C * 128, 1024);
-#pragma unroll
-                for (int s = 0; s < C / 16; ++s)
-                    umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 2048), id_mm, s > 0);
-                umma_commit(&bar[3]);
-                // ... then D1[b] += [x; P] U (outputs only), which runs while S is updated
                 const uint64_t azp = sdesc_sw128(bufa + REC_P - 8192, 16, 1024);
+                if (elect_one()) {
 #pragma unroll
-                for (int s = 0; s < C / 16; ++s)
-                    umma_bf16(tmem + 128 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 2048), id_km, 1);
-                umma_commit(&bar[4]);
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 2048), id_mm, s > 0);
+                    umma_commit(&bar[3]);
+                    // ... then D1[b] += [x; P] U (outputs only), which runs while S is updated
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(tmem + 128 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 2048), id_km, 1);
+                    umma_commit(&bar[4]);
+                }
+                __syncwarp();
             }
             ok = mbar_wait(&bar[3], gi & 1);
             tc_fence_after();

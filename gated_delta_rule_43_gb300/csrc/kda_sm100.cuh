@@ -121,6 +121,19 @@ __device__ __forceinline__ void fence_proxy_async() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// True in exactly one lane of a converged warp (elect.sync over the full mask).  Issuing
+// tcgen05 operations from the elected lane of a converged warp keeps the operands'
+// warp-uniform values in uniform registers.
+__device__ __forceinline__ bool elect_one() {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 l;\n\t"
+        "elect.sync l|p, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r));
+    return r != 0;
+}
+
 // Named barrier `id` over `n` threads (a multiple of 32) that also ANDs a predicate
 // across them: every participant gets the same answer.
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {

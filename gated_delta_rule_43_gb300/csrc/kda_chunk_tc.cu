@@ -855,25 +855,28 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 __syncwarp();
             }
             if (warp < 2) {
-                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
+                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1).  While the
+                // product runs: this thread's row of Ut into registers, and the wait for the
+                // previous chunk's [x; P] U product, the last reader of the U image.
+                const int r = tid;
+                const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
+                float4 u4[8];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) u4[j4] = ut[j4 ^ (r & 7)];
+                if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                 ok = ok && mbar_wait(&bar[2], gi & 1);
                 tc_fence_after();
                 if (ok) {
-                    const int r = tid;
                     float acc[32];
                     tmem_ld32(tmem + 32 * b + lane_base, acc);
                     tmem_ld_wait();
-                    const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 u4 = ut[j4 ^ (r & 7)];
-                        acc[4 * j4 + 0] = u4.x - acc[4 * j4 + 0];
-                        acc[4 * j4 + 1] = u4.y - acc[4 * j4 + 1];
-                        acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
-                        acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
+                        acc[4 * j4 + 0] = u4[j4].x - acc[4 * j4 + 0];
+                        acc[4 * j4 + 1] = u4[j4].y - acc[4 * j4 + 1];
+                        acc[4 * j4 + 2] = u4[j4].z - acc[4 * j4 + 2];
+                        acc[4 * j4 + 3] = u4[j4].w - acc[4 * j4 + 3];
                     }
-                    // the U image is free once the previous chunk's [x; P] U product is done
-                    if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                     store_row_sw64(sm + C_UI, r, acc);
                 }
                 fence_proxy_async();
@@ -908,10 +911,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 }
             }
             // S <- Diag(Gam_C) S + D2 (row i = tid)
+            const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
             ok = mbar_wait(&bar[3], gi & 1) && ok;
             tc_fence_after();
             if (ok) {
-                const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
                 float acc[32];
                 tmem_ld32(D2 + lane_base, acc);
                 tmem_ld_wait();

@@ -367,9 +367,10 @@ def decode_bench(args, dev, stream, world, pk, pk_src):
 
 def e2e_bench(args, d, dev, stream, world):
     """Same prefill metric through the public call with pinned host buffers: H2D of every
-    input and D2H of o and the final state inside the timed region, every step.  Steps
-    alternate between two streams with their own device buffers, so that the copies of
-    one step overlap the compute of the other (what a caller streaming batches does)."""
+    input and D2H of o and the final state inside the timed region, every step.  What a
+    caller streaming batches does: the host-to-device copies run back to back on their
+    own stream (the host link is the bound), compute and device-to-host copies on two
+    more, with two sets of device buffers and events between the three."""
     import torch
 
     from gated_delta_rule_43_gb300 import kda
@@ -380,30 +381,41 @@ def e2e_bench(args, d, dev, stream, world):
     N = d["cu_seqlens"].numel() - 1
     dk = d["q"].shape[2]
     ws_bytes = kda.chunk_fwd_workspace_size(T, N, H, dk, dv, d["q"].dtype)
+    s_in, s_comp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev = lambda: torch.cuda.Event()
     lanes = []
     for _ in range(2):
         lanes.append({
-            "s": torch.cuda.Stream(dev),
             "dev": {n: torch.empty_like(d[n]) for n in names},
             "o": torch.empty(T, H, dv, dtype=d["q"].dtype, device=dev),
             "hT": torch.empty(N, H, dk, dv, dtype=torch.float32, device=dev),
             "o_h": torch.empty((T, H, dv), dtype=d["q"].dtype).pin_memory(),
             "s_h": torch.empty((N, H, dk, dv), dtype=torch.float32).pin_memory(),
             "ws": kda.alloc_workspace(ws_bytes, dev),
+            "loaded": ev(), "computed": ev(), "copied_out": ev(),
         })
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = lanes[0]["o"].numel() * lanes[0]["o"].element_size() + lanes[0]["hT"].numel() * 4
 
     def step(i):
         L = lanes[i % 2]
-        with torch.cuda.stream(L["s"]):
+        b = L["dev"]
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(L["computed"])          # step i - 2 has read these inputs
             for n in names:
-                L["dev"][n].copy_(host[n], non_blocking=True)
-            b = L["dev"]
+                b[n].copy_(host[n], non_blocking=True)
+            L["loaded"].record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(L["loaded"])
+            s_comp.wait_event(L["copied_out"])      # step i - 2's outputs have left
             kda.chunk_fwd(b["q"], b["k"], b["v"], b["z"], b["beta"], b["A_log"], b["cu_seqlens"],
-                          None, o=L["o"], final_state=L["hT"], workspace=L["ws"], stream=L["s"])
+                          None, o=L["o"], final_state=L["hT"], workspace=L["ws"], stream=s_comp)
+            L["computed"].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(L["computed"])
             L["o_h"].copy_(L["o"], non_blocking=True)
             L["s_h"].copy_(L["hT"], non_blocking=True)
+            L["copied_out"].record(s_out)
 
     for i in range(2):
         step(i)
@@ -412,12 +424,12 @@ def e2e_bench(args, d, dev, stream, world):
     barrier(world)
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     s.record(stream)
-    for L in lanes:
-        L["s"].wait_stream(stream)
+    for x in (s_in, s_comp, s_out):
+        x.wait_stream(stream)
     for i in range(K):
         step(i)
-    for L in lanes:
-        stream.wait_stream(L["s"])
+    for x in (s_in, s_comp, s_out):
+        stream.wait_stream(x)
     e.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
@@ -426,8 +438,9 @@ def e2e_bench(args, d, dev, stream, world):
     val, _ = aggregate(T * K, s.elapsed_time(e) / 1e3, world)
     return {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
-            "note": "two streams, double-buffered device inputs: copies of one step overlap "
-                    "the compute of the next"}
+            "note": "H2D, compute and D2H on three streams with two sets of device buffers: "
+                    "the next step's inputs stream in while this step computes and its "
+                    "outputs stream out"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

@@ -16,7 +16,8 @@ namespace kda {
 // kernel of a call, so nothing has reported yet).  With S_run != NULL every CTA also
 // gives each sequence that owns no chunk (empty or invalid) its final state: h0's
 // (zeros when h0 is NULL) -- the chunk kernels only write states of sequences they walk.
-__global__ void __launch_bounds__(1024)
+constexpr int PLAN_THREADS = 256;
+__global__ void __launch_bounds__(PLAN_THREADS)
 plan_chunks_kernel(const int32_t *__restrict__ cu, int N, int64_t T_tot, int C,
                    int32_t *__restrict__ chunk_off, StatusWord *st, int clear_status,
                    const float *__restrict__ h0, float *__restrict__ S_run, int H,
@@ -33,14 +34,14 @@ plan_chunks_kernel(const int32_t *__restrict__ cu, int N, int64_t T_tot, int C,
         }
     }
     if (blockIdx.x != 0) return;
-    __shared__ int32_t s_warp[32];
+    constexpr int NW = PLAN_THREADS / 32;
+    __shared__ int32_t s_warp[NW];
     __shared__ int32_t s_carry;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
     if (clear_status && tid == 0) {
         st->code = 0u;
         st->site = 0u;
         st->info = 0ull;
-        __threadfence();
     }
     __syncthreads();
     if (tid == 0) {
@@ -48,7 +49,7 @@ plan_chunks_kernel(const int32_t *__restrict__ cu, int N, int64_t T_tot, int C,
         if (cu[0] != 0 || (int64_t)cu[N] != T_tot) report(st, KDA_ERR_SEQLENS, N, 1);
     }
     __syncthreads();
-    for (int base = 0; base < N; base += 1024) {
+    for (int base = 0; base < N; base += PLAN_THREADS) {
         const int n = base + tid;
         int32_t cnt = 0;
         if (n < N) {
@@ -68,19 +69,19 @@ plan_chunks_kernel(const int32_t *__restrict__ cu, int N, int64_t T_tot, int C,
         if (lane == 31) s_warp[wid] = x;
         __syncthreads();
         if (wid == 0) {
-            int32_t w = s_warp[lane];
+            int32_t w = lane < NW ? s_warp[lane] : 0;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
+            for (int o = 1; o < NW; o <<= 1) {
                 const int32_t y = __shfl_up_sync(0xffffffffu, w, o);
                 if (lane >= o) w += y;
             }
-            s_warp[lane] = w;
+            if (lane < NW) s_warp[lane] = w;
         }
         __syncthreads();
         const int32_t incl = x + (wid > 0 ? s_warp[wid - 1] : 0) + s_carry;
         if (n < N) chunk_off[n] = incl - cnt;
         __syncthreads();
-        if (tid == 1023) s_carry = incl;
+        if (tid == PLAN_THREADS - 1) s_carry = incl;
         __syncthreads();
     }
     if (tid == 0) chunk_off[N] = s_carry;
@@ -136,7 +137,7 @@ __global__ void gate_cumsum_kernel(const T *__restrict__ z, const float *__restr
 
 cudaError_t launch_plan(const int32_t *cu, int N, int64_t T_tot, int C, int32_t *chunk_off,
                         StatusWord *st, cudaStream_t s) {
-    plan_chunks_kernel<<<1, 1024, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 0, nullptr, nullptr,
+    plan_chunks_kernel<<<1, PLAN_THREADS, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 0, nullptr, nullptr,
                                           0, 0);
     return cudaGetLastError();
 }
@@ -147,7 +148,7 @@ cudaError_t launch_plan_tc(const int32_t *cu, int N, int64_t T_tot, int C, int32
                            StatusWord *st, const float *h0, float *S_run, int H, int64_t dkdv,
                            int grid, cudaStream_t s) {
     const bool init = S_run != h0;
-    plan_chunks_kernel<<<init ? grid : 1, 1024, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 1, h0,
+    plan_chunks_kernel<<<init ? grid : 1, PLAN_THREADS, 0, s>>>(cu, N, T_tot, C, chunk_off, st, 1, h0,
                                                        init ? S_run : nullptr, H, dkdv / 4);
     return cudaGetLastError();
 }

@@ -144,6 +144,11 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
     return L > 0;
 }
 
+// Window-relative chunk slot of the prep CTA at position y of the launch's slot
+// dimension: the last slots first, so that the records of a window's first chunks, which
+// the chain kernel reads first, are the most recently written (still in L2).
+__device__ __forceinline__ int32_t prep_slot(int32_t y, int32_t nslots) { return nslots - 1 - y; }
+
 // One CTA per (chunk slot, head).  Work split for the row-wise element passes: lane l of
 // warp w takes the 8-channel chunk ch = 2w + (l >> 4) of rows 16u + (l & 15), one in each
 // 16-token tile u = 0..3.  The in-tile cumulative sums run down the columns of a
@@ -159,12 +164,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int32_t slot = slot0 + (int32_t)blockIdx.x;
-    const int h = blockIdx.y;
+    // launch order is slot-major (all heads of a chunk slot, then the previous slot): the
+    // CTAs of a wave read whole token rows of q, k, z and v
+    const int32_t xs = prep_slot((int32_t)blockIdx.y, (int32_t)gridDim.y);
+    const int32_t slot = slot0 + xs;
+    const int h = blockIdx.x;
     int n = 0, L = 0;
     int64_t t0 = 0;
     if (!slot_chunk(cu, chunk_off, N, slot, n, t0, L)) return;
-    uint8_t *rec = records + ((size_t)blockIdx.x * H + h) * REC_BYTES;
+    uint8_t *rec = records + ((size_t)xs * H + h) * REC_BYTES;
 
     float *TOT = reinterpret_cast<float *>(sm + P_TOT);
     float *ER = reinterpret_cast<float *>(sm + P_ER);
@@ -212,11 +220,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         int n2 = 0, L2 = 0;
         int64_t t2 = 0;
         if (lin < (int64_t)gridDim.x * gridDim.y &&
-            slot_chunk(cu, chunk_off, N, slot0 + (int32_t)(lin % gridDim.x), n2, t2, L2)) {
+            slot_chunk(cu, chunk_off, N, slot0 + prep_slot((int32_t)(lin / gridDim.x), (int32_t)gridDim.y),
+                       n2, t2, L2)) {
             const int tsel = (tid >> 6) & 3, rr = tid & 63;
             const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
             if (tid < 256 && rr < L2) {
-                const __nv_bfloat16 *row = src + ((t2 + rr) * H + (int)(lin / gridDim.x)) * (int64_t)DK;
+                const __nv_bfloat16 *row = src + ((t2 + rr) * H + (int)(lin % gridDim.x)) * (int64_t)DK;
                 prefetch_l2(row);
                 prefetch_l2(row + 64);
             }
@@ -1305,6 +1314,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec) {
     using namespace tc;
+    if (window > 65535) return cudaErrorInvalidValue;   // the prep grid's slot dimension
     CUtensorMap tmap_q, tmap_k, tmap_z, tmap_v;
     if (T_tot > 0) {
         cudaError_t te = tmap_thd(&tmap_q, q, T_tot, H);
@@ -1358,7 +1368,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
             e = cudaStreamWaitEvent(sp, P->chain_done[par], 0);
             if (e != cudaSuccess) return e;
         }
-        dim3 pg((unsigned)(s1 - s0), (unsigned)H);
+        dim3 pg((unsigned)H, (unsigned)(s1 - s0));   // slot-major; a window holds < 65536 slots
         if (rec) rec->mark(sp);
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,

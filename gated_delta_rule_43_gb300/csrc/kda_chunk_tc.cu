@@ -654,7 +654,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
             bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
             bulk_commit();
-            bulk_wait_all();
+            // the CTA may leave once the staging has been read; the writes complete with
+            // the kernel, before anything ordered after it reads the records
+            bulk_wait_read_all();
         }
     }
 }

@@ -28,6 +28,13 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
                             const float *h0, float *S_run, void *o, uint8_t *records,
                             int64_t window, int nbuf, StatusWord *st, cudaStream_t s,
                             EventRec *rec);
+cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *v,
+                                      const void *z, const void *beta, const float *A_log,
+                                      const int32_t *cu, const int32_t *chunk_off, int N,
+                                      int64_t T_tot, int64_t slots, int H, const float *h0,
+                                      float *S_run, void *o, uint8_t *records, int64_t window,
+                                      int segs, float *start, float *maps, StatusWord *st,
+                                      cudaStream_t s);
 int64_t chunk_slots(int64_t T_tot, int N, int C);
 cudaError_t launch_gate(int dtype, const void *z, const float *A_log, const int32_t *cu,
                         const int32_t *chunk_off, int N, int64_t T_tot, int H, int dk, int C,
@@ -64,6 +71,9 @@ struct ChunkLayout {
     size_t rec_off, rec_bytes;       // one or two windows of chunk records
     int64_t slots, window;
     int nbuf;                        // record buffers: 2 when there is more than one window
+    size_t seg_off, seg_bytes;       // segmented schedule: segment start states
+    size_t map_off, map_bytes;       //   and [M | B] maps
+    int segs;                        // segments per sequence and window (1: plain schedule)
     size_t total;
 };
 
@@ -90,7 +100,32 @@ ChunkLayout chunk_layout(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv
         }
         L.rec_bytes = (size_t)L.nbuf * L.window * rec;
     }
+    L.segs = 1;
+    L.seg_off = L.map_off = L.rec_off + L.rec_bytes;
+    L.seg_bytes = L.map_bytes = 0;
     L.total = L.rec_off + L.rec_bytes;
+    return L;
+}
+
+// The segment-parallel schedule runs its windows one after the other (one record
+// buffer) and adds the start states and maps of the later segments.
+ChunkLayout chunk_layout_seg(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv,
+                             int32_t dtype, int32_t segs) {
+    ChunkLayout L = chunk_layout(T, N, H, dk, dv, dtype);
+    if (segs <= 1 || !use_tc(dtype, dk, dv)) return L;
+    const size_t rec = tc_record_bytes() * (size_t)H;
+    int64_t w = (int64_t)(kTcRecordBudget / rec);
+    if (w < 1) w = 1;
+    L.window = L.slots < w ? L.slots : w;
+    L.nbuf = 1;
+    L.rec_bytes = (size_t)L.window * rec;
+    L.segs = segs;
+    const size_t pairs = (size_t)N * H * segs;
+    L.seg_off = L.rec_off + L.rec_bytes;
+    L.seg_bytes = round_up(pairs * dk * dv * sizeof(float), 1024);
+    L.map_off = L.seg_off + L.seg_bytes;
+    L.map_bytes = round_up(pairs * dk * (dk + dv) * sizeof(float), 1024);
+    L.total = L.map_off + L.map_bytes;
     return L;
 }
 
@@ -108,7 +143,7 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
                           int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t dk,
                           int32_t dv, int32_t dtype, const float *initial_state,
                           float *final_state, void *o, void *workspace, size_t workspace_bytes,
-                          void *stream, EventRec *rec) {
+                          void *stream, EventRec *rec, int32_t segs = 1) {
     if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_UNSUPPORTED;
     if (!head_ok(dk) || !head_ok(dv)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs < 0 || total_tokens < 0 || H <= 0) return KDA_ERR_INVALID_ARG;
@@ -122,7 +157,8 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
         if (!aligned(p, 16)) return KDA_ERR_INVALID_ARG;
     if (!aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
     if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
-    const ChunkLayout L = chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype);
+    if (segs < 1 || segs > 64) return KDA_ERR_INVALID_ARG;
+    const ChunkLayout L = chunk_layout_seg(total_tokens, num_seqs, H, dk, dv, dtype, segs);
     if (workspace_bytes < L.total) return KDA_ERR_INVALID_ARG;
     if (chunk_slots_overflow(total_tokens, num_seqs, kTcChunk)) return KDA_ERR_INVALID_ARG;
     // token coordinates of the tensor-core path's tile loads are 32-bit
@@ -144,10 +180,17 @@ kda_status chunk_fwd_impl(const void *q, const void *k, const void *v, const voi
                            s);
         if (e != cudaSuccess) return KDA_ERR_CUDA;
         if (rec) rec->mark(s);
-        e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
-                            total_tokens, L.slots, H,
-                            initial_state, S_run, o, ws + L.rec_off, L.window, L.nbuf, st, s,
-                            rec);
+        if (L.segs > 1)
+            e = launch_chunk_tc_segmented(q, k, v, z, beta, A_log, cu_seqlens, chunk_off,
+                                          num_seqs, total_tokens, L.slots, H, initial_state,
+                                          S_run, o, ws + L.rec_off, L.window, L.segs,
+                                          (float *)(ws + L.seg_off), (float *)(ws + L.map_off),
+                                          st, s);
+        else
+            e = launch_chunk_tc(q, k, v, z, beta, A_log, cu_seqlens, chunk_off, num_seqs,
+                                total_tokens, L.slots, H,
+                                initial_state, S_run, o, ws + L.rec_off, L.window, L.nbuf, st, s,
+                                rec);
         return cuda_status(e);
     }
     e = cudaMemsetAsync(st, 0, sizeof(StatusWord), s);
@@ -186,6 +229,15 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
     return chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype).total;
 }
 
+size_t kda_chunk_fwd_segmented_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
+                                              int32_t dk, int32_t dv, int32_t dtype,
+                                              int32_t segments) {
+    if (total_tokens < 0 || num_seqs < 0 || H <= 0 || !head_ok(dk) || !head_ok(dv) ||
+        (dtype != KDA_F32 && dtype != KDA_BF16) || segments < 1 || segments > 64)
+        return 0;
+    return chunk_layout_seg(total_tokens, num_seqs, H, dk, dv, dtype, segments).total;
+}
+
 size_t kda_decode_workspace_size(void) { return kHeaderBytes; }
 
 kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void *z,
@@ -197,6 +249,18 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
     return chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
                           dtype, initial_state, final_state, o, workspace, workspace_bytes, stream,
                           nullptr);
+}
+
+kda_status kda_chunk_fwd_segmented(const void *q, const void *k, const void *v, const void *z,
+                                   const void *beta, const float *A_log,
+                                   const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t dtype, const float *initial_state, float *final_state,
+                                   void *o, int32_t segments, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    return chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
+                          dtype, initial_state, final_state, o, workspace, workspace_bytes, stream,
+                          nullptr, segments);
 }
 
 kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, const void *z,

@@ -674,6 +674,28 @@ __device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32
     return lo;
 }
 
+// Segment-parallel passes (the pages' KDA context parallelism, P2 "Infrastructure and
+// Training/Inference Mechanics", applied to segments of one window instead of ranks):
+// mode 1 walks segment 0 of every sequence from its state and, at the same time, every
+// later segment from [I | 0] with [0 | Ut], which yields that segment's affine map
+// S_end = M S_start + B (M evolves like S with V = 0); a scan composes the maps into each
+// later segment's start state; mode 2 then walks the later segments from those states.
+// Mode 0 is the plain walk.
+struct SegArgs {
+    int mode;       // 0 plain, 1 first pass, 2 second pass
+    int segs;       // segments per sequence and window (>= 2 in modes 1 and 2)
+    float *start;   // [N][H][segs][DK][DV]      start state of segment k >= 1
+    float *maps;    // [N][H][segs][DK][DK + DV] [M | B] of segment k >= 1
+};
+// Chunks [b, e) of segment k when a sequence's L chunks of the window, starting at c0,
+// are cut into s_eff = min(segs, L) near-equal segments.
+__device__ __forceinline__ void seg_range(int32_t c0, int32_t L, int segs, int k, int32_t &b,
+                                          int32_t &e, int &s_eff) {
+    s_eff = min(segs, (int)L);
+    b = c0 + (int32_t)(((int64_t)k * L) / s_eff);
+    e = c0 + (int32_t)(((int64_t)(k + 1) * L) / s_eff);
+}
+
 // ------------------------------------------------ chain kernel, 32-column blocks
 // The latency-bound shape: one CTA per (sequence, head, 32-column block of dv).  The
 // N = 32 products finish sooner than N = 128 ones, so a lone long sequence walks its
@@ -681,6 +703,7 @@ __device__ __forceinline__ int slot_owner(const int32_t *chunk_off, int N, int32
 namespace c32 {
 
 constexpr int DVB = 32;          // value columns per CTA
+constexpr int DK_ROWS = DK;      // threads of the scan kernel (one per state row)
 constexpr int NBLK = DV / DVB;
 constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x; P] U
 // a record buffer mirrors the record's first 57344 bytes (WQ, KT, P), then this CTA's U
@@ -728,7 +751,7 @@ __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
              const float *h0, float *__restrict__ state, __nv_bfloat16 *__restrict__ o,
-             StatusWord *st) {
+             StatusWord *st, SegArgs sa) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -736,7 +759,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     if (slot0 >= used) return;
     const int n_first = slot_owner(chunk_off, N, slot0);
     const int n_last = slot_owner(chunk_off, N, used - 1);
-    const int items = (n_last - n_first + 1) * H * NBLK;
+    // items per (sequence, head): the column blocks, and in mode 1 the 2 NBLK blocks of
+    // [M | B] of every later segment, in mode 2 the blocks of every later segment
+    const int ipp = sa.mode == 0 ? NBLK
+                  : sa.mode == 1 ? NBLK + 2 * NBLK * (sa.segs - 1) : NBLK * (sa.segs - 1);
+    const int items = (n_last - n_first + 1) * H * ipp;
     if ((int)blockIdx.x >= items) return;
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3
@@ -766,28 +793,57 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
     for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
-        const int blk = item % NBLK;
-        const int h = (item / NBLK) % H;
-        const int n = n_first + item / (NBLK * H);
+        const int r_it = item % ipp;
+        const int h = (item / ipp) % H;
+        const int n = n_first + item / (ipp * H);
+        int blk = r_it, seg = 0;
+        bool map = false, mpart = false;   // an [M | B] item, and of the M columns
+        if (sa.mode == 1 && r_it >= NBLK) {
+            const int x = r_it - NBLK;
+            seg = 1 + x / (2 * NBLK);
+            map = true;
+            mpart = x % (2 * NBLK) < NBLK;
+            blk = x % NBLK;
+        } else if (sa.mode == 2) {
+            seg = 1 + r_it / NBLK;
+            blk = r_it % NBLK;
+        }
         const int32_t cfirst = chunk_off[n];
-        const int32_t c_begin = max(cfirst, slot0);
-        const int32_t c_end = min(chunk_off[n + 1], slot1);
+        const int32_t w_begin = max(cfirst, slot0);
+        int32_t c_begin = w_begin;
+        int32_t c_end = min(chunk_off[n + 1], slot1);
         if (c_begin >= c_end) continue;
+        int s_eff = 1;
+        if (sa.mode != 0) {
+            int32_t sb = 0, se = 0;
+            seg_range(w_begin, c_end - w_begin, sa.segs, seg, sb, se, s_eff);
+            if (seg >= s_eff) continue;
+            c_begin = sb;
+            c_end = se;
+        }
         const int64_t bos = cu[n];
         const int64_t eos = cu[n + 1];
         const int j0 = blk * DVB;
         float S[DVB];
-        const int64_t soff = (((int64_t)n * H + h) * DK + i) * DV + j0;
+        const int64_t pairoff = (int64_t)n * H + h;
+        const int64_t soff = (pairoff * DK + i) * DV + j0;
         float *srow = state + soff;
         // the sequence's first chunk starts from h0 (zeros when absent), later windows from
-        // the running state
-        const float *s_in = c_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
+        // the running state, a later segment from its composed start state, a map from
+        // the identity (M columns) or zeros (B columns)
+        const float *s_in = map ? nullptr
+                          : seg > 0 ? sa.start + ((pairoff * sa.segs + seg) * DK + i) * DV + j0
+                          : w_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
         if (warp < 4) {
 #pragma unroll
             for (int j4 = 0; j4 < DVB / 4; ++j4) {
                 const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+            }
+            if (mpart) {
+#pragma unroll
+                for (int j = 0; j < DVB; ++j) S[j] = (i == j0 + j) ? 1.f : 0.f;
             }
             store_row_sw64(sm + C_S, i, S);
             fence_proxy_async();
@@ -809,7 +865,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             float oacc[32];
             tmem_ld32(tmem + 32 * pb + lane_base, oacc);
             tmem_ld_wait();
-            if (t < eos) {
+            if (t < eos && !map) {
                 uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
 #pragma unroll
                 for (int i8 = 0; i8 < 4; ++i8) {
@@ -873,7 +929,8 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
                 float4 u4[8];
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4) u4[j4] = ut[j4 ^ (r & 7)];
+                for (int j4 = 0; j4 < 8; ++j4)   // the M columns of a map see Ut = 0
+                    u4[j4] = mpart ? make_float4(0.f, 0.f, 0.f, 0.f) : ut[j4 ^ (r & 7)];
                 if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1)) ok = false;
                 ok = ok && mbar_wait(&bar[2], gi & 1);
                 tc_fence_after();
@@ -950,10 +1007,20 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             bool ok_o = true;
             if (warp >= 2 && warp < 4) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
             if (!ok_o) *abort_flag = 1;
-            if (warp < 4) {
+            // where the walk's end state goes: the running state, segment 1's start (first
+            // pass, segment 0), the map, or nowhere (second pass, all but the last segment:
+            // their ends are the next segments' composed starts)
+            float *dst = srow;
+            if (map)
+                dst = sa.maps + ((pairoff * sa.segs + seg) * DK + i) * (DK + DV) + (mpart ? 0 : DK) + j0;
+            else if (sa.mode == 1 && s_eff > 1)
+                dst = sa.start + ((pairoff * sa.segs + 1) * DK + i) * DV + j0;
+            else if (sa.mode == 2 && seg != s_eff - 1)
+                dst = nullptr;
+            if (warp < 4 && dst) {
 #pragma unroll
                 for (int j4 = 0; j4 < DVB / 4; ++j4)
-                    reinterpret_cast<float4 *>(srow)[j4] =
+                    reinterpret_cast<float4 *>(dst)[j4] =
                         make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
             }
         }
@@ -964,6 +1031,71 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 128);
+    }
+}
+
+
+// The scan of the segment-parallel schedule: for every (sequence, head, 32-column block)
+// of the window, start(k + 1) = M_k start(k) + B_k for k = 1 .. s_eff - 2 (start(1) is
+// segment 0's end state from the first pass).  fp32; thread i = row i.
+__global__ void __launch_bounds__(DK)
+seg_scan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
+                int H, int32_t slot0, int32_t slot1, SegArgs sa) {
+    __shared__ __align__(16) float Ss[DK][DVB];
+    const int i = threadIdx.x;
+    const int32_t used = min(slot1, chunk_off[N]);
+    if (slot0 >= used) return;
+    const int n_first = slot_owner(chunk_off, N, slot0);
+    const int n_last = slot_owner(chunk_off, N, used - 1);
+    const int items = (n_last - n_first + 1) * H * NBLK;
+    for (int item = blockIdx.x; item < items; item += gridDim.x) {
+        const int blk = item % NBLK;
+        const int h = (item / NBLK) % H;
+        const int n = n_first + item / (NBLK * H);
+        const int32_t c_begin = max(chunk_off[n], slot0);
+        const int32_t c_end = min(chunk_off[n + 1], slot1);
+        const int L = c_end - c_begin;
+        const int s_eff = min(sa.segs, L);
+        if (s_eff < 3) continue;
+        const int j0 = blk * DVB;
+        const int64_t pairoff = (int64_t)n * H + h;
+        float S[DVB];
+        {
+            const float4 *src = reinterpret_cast<const float4 *>(
+                sa.start + ((pairoff * sa.segs + 1) * DK + i) * DV + j0);
+#pragma unroll
+            for (int j4 = 0; j4 < DVB / 4; ++j4) {
+                const float4 x = src[j4];
+                S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+            }
+        }
+        for (int k = 1; k + 1 < s_eff; ++k) {
+            __syncthreads();   // the previous step's reads of Ss are done
+#pragma unroll
+            for (int j = 0; j < DVB; ++j) Ss[i][j] = S[j];
+            __syncthreads();
+            const float *mrow = sa.maps + ((pairoff * sa.segs + k) * DK + i) * (DK + DV);
+            float acc[DVB];
+#pragma unroll
+            for (int j = 0; j < DVB; ++j) acc[j] = mrow[DK + j0 + j];
+            for (int m4 = 0; m4 < DK / 4; ++m4) {
+                const float4 mv = reinterpret_cast<const float4 *>(mrow)[m4];
+                const float mm[4] = {mv.x, mv.y, mv.z, mv.w};
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+#pragma unroll
+                    for (int j = 0; j < DVB; ++j) acc[j] += mm[t] * Ss[4 * m4 + t][j];
+                }
+            }
+            float4 *dst = reinterpret_cast<float4 *>(
+                sa.start + ((pairoff * sa.segs + k + 1) * DK + i) * DV + j0);
+#pragma unroll
+            for (int j4 = 0; j4 < DVB / 4; ++j4) {
+                dst[j4] = make_float4(acc[4 * j4], acc[4 * j4 + 1], acc[4 * j4 + 2], acc[4 * j4 + 3]);
+                S[4 * j4] = acc[4 * j4]; S[4 * j4 + 1] = acc[4 * j4 + 1];
+                S[4 * j4 + 2] = acc[4 * j4 + 2]; S[4 * j4 + 3] = acc[4 * j4 + 3];
+            }
+        }
     }
 }
 
@@ -1394,7 +1526,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
             const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
             c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, sc>>>(
                 cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,
-                (__nv_bfloat16 *)o, st);
+                (__nv_bfloat16 *)o, st, SegArgs{0, 1, nullptr, nullptr});
         } else {
             const int64_t grid = std::min<int64_t>(seqs * H, sm_count);
             c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, sc>>>(
@@ -1411,6 +1543,62 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         e = cudaEventRecord(P->end, P->chain);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, P->end, 0);
         if (e != cudaSuccess) return e;
+    }
+    return cudaGetLastError();
+}
+
+// The segment-parallel schedule (see SegArgs): per window of records, on `s` alone: prep,
+// first pass (segment 0 walked, later segments' maps), scan, second pass.  Always the
+// 32-column chain; `start` and `maps` hold N x H x segs blocks of the shapes in SegArgs.
+cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *v,
+                                      const void *z, const void *beta, const float *A_log,
+                                      const int32_t *cu, const int32_t *chunk_off, int N,
+                                      int64_t T_tot, int64_t slots, int H, const float *h0,
+                                      float *S_run, void *o, uint8_t *records, int64_t window,
+                                      int segs, float *start, float *maps, StatusWord *st,
+                                      cudaStream_t s) {
+    using namespace tc;
+    if (window > 65535 || segs < 2) return cudaErrorInvalidValue;
+    CUtensorMap tmap_q, tmap_k, tmap_z, tmap_v;
+    if (T_tot > 0) {
+        cudaError_t te = tmap_thd(&tmap_q, q, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_k, k, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_z, z, T_tot, H);
+        if (te == cudaSuccess) te = tmap_thd(&tmap_v, v, T_tot, H);
+        if (te != cudaSuccess) return te;
+    } else {
+        return cudaSuccess;
+    }
+    cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)P_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(c32::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)c32::C_SMEM);
+    int dev = 0, sm_count = 0;
+    if (e == cudaSuccess) e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    for (int64_t s0 = 0; s0 < slots; s0 += window) {
+        const int64_t s1 = std::min(slots, s0 + window);
+        dim3 pg((unsigned)H, (unsigned)(s1 - s0));
+        prep_kernel<<<pg, PREP_THREADS, P_SMEM, s>>>(
+            (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
+            (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
+            (int32_t)s0, records, st, 2 * sm_count, tmap_q, tmap_k, tmap_z, tmap_v);
+        const int64_t pairs = std::min<int64_t>(N, s1 - s0) * H;
+        const int64_t items1 = pairs * (c32::NBLK + 2 * c32::NBLK * (segs - 1));
+        c32::chain_kernel<<<(unsigned)std::min<int64_t>(items1, sm_count), c32::CHAIN_THREADS,
+                            c32::C_SMEM, s>>>(cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1,
+                                              records, h0, S_run, (__nv_bfloat16 *)o, st,
+                                              SegArgs{1, segs, start, maps});
+        c32::seg_scan_kernel<<<(unsigned)std::min<int64_t>(pairs * c32::NBLK, 4 * sm_count),
+                               c32::DK_ROWS, 0, s>>>(cu, chunk_off, N, H, (int32_t)s0,
+                                                      (int32_t)s1, SegArgs{1, segs, start, maps});
+        const int64_t items2 = pairs * c32::NBLK * (segs - 1);
+        c32::chain_kernel<<<(unsigned)std::min<int64_t>(items2, sm_count), c32::CHAIN_THREADS,
+                            c32::C_SMEM, s>>>(cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1,
+                                              records, h0, S_run, (__nv_bfloat16 *)o, st,
+                                              SegArgs{2, segs, start, maps});
     }
     return cudaGetLastError();
 }

@@ -88,12 +88,16 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 
 
 def make_prefill(seqlens, H: int, dk: int, dv: int, dtype: str = "bf16", *, seed: int = 0,
-                 h0_sigma: float = 0.0, device="cpu", gen: torch.Generator | None = None):
+                 h0_sigma: float = 0.0, z_shift: float = 0.0, device="cpu",
+                 gen: torch.Generator | None = None):
     """Packed prefill inputs.  Returns a dict of tensors on `device`:
 
     q, k, z [T, H, dk] and v [T, H, dv] in `dtype`; beta [T, H] in `dtype`;
     A_log [H] fp32; cu_seqlens [N+1] int32; h0 [N, H, dk, dv] fp32 or None.
     `seqlens` may be a list of lengths or a ("uniform", count, lo, hi) spec.
+    z ~ N(z_shift, 1): the default centres the gate near g = -2.5 (the state keeps a
+    token for about one step); z_shift = -4 gives g near -0.05 per token, a memory of
+    tens to hundreds of tokens, across many chunks.
     """
     gen = gen or _gen(seed, device)
     lens = draw_seqlens(tuple(seqlens), gen)
@@ -104,7 +108,7 @@ def make_prefill(seqlens, H: int, dk: int, dv: int, dtype: str = "bf16", *, seed
     q = _unit_rows(torch.randn(T, H, dk, **f32)) * (1.0 / math.sqrt(dk))
     k = _unit_rows(torch.randn(T, H, dk, **f32))
     v = torch.randn(T, H, dv, **f32)
-    z = torch.randn(T, H, dk, **f32)
+    z = torch.randn(T, H, dk, **f32) + z_shift
     A = torch.rand(H, **f32) * 2.0 - 1.0
     beta = torch.sigmoid(torch.randn(T, H, **f32))
     h0 = torch.randn(N, H, dk, dv, **f32) * h0_sigma if h0_sigma > 0 else None

@@ -32,6 +32,9 @@ SIGNATURES = {
     "kda_chunk_fwd_profiled": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P,
                                      P, P, SZ, P, ctypes.POINTER(ctypes.c_void_p), I32,
                                      ctypes.POINTER(ctypes.c_int32)]),
+    "kda_chunk_fwd_segmented_workspace_size": (SZ, [I64, I32, I32, I32, I32, I32, I32]),
+    "kda_chunk_fwd_segmented": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P,
+                                      P, I32, P, SZ, P]),
     "kda_chunk_fwd_noalloc": (I32, [P, P, P, P, P, P, P, I32, I64, I32, I32, I32, I32, P, P, P,
                                     P, P]),
     "kda_decode_workspace_size": (SZ, []),
@@ -141,6 +144,38 @@ def chunk_fwd(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None, *,
                            _stream(stream))
     if rc != KDA_OK:
         raise KdaError(rc, "kda_chunk_fwd")
+    if check:
+        query_status(workspace, stream, raise_on_error=True)
+    return o, final_state
+
+
+def chunk_fwd_segmented(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None, *,
+                        segments: int, output_final_state: bool = True, o=None,
+                        final_state=None, workspace=None, stream=None, check: bool = False):
+    """Segment-parallel prefill (kda_chunk_fwd_segmented): chunk_fwd's arguments and
+    results, each sequence's chunks of a window cut into up to ``segments`` segments."""
+    lib = load()
+    _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
+    T, H, dk = q.shape
+    dv = v.shape[-1]
+    N = cu_seqlens.numel() - 1
+    dt = _DT[q.dtype]
+    if A_log.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("A_log must be fp32 and cu_seqlens int32")
+    if o is None:
+        o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, H, dk, dv, dtype=torch.float32, device=q.device)
+    need = int(lib.kda_chunk_fwd_segmented_workspace_size(T, N, H, dk, dv, dt, int(segments)))
+    if workspace is None:
+        workspace = alloc_workspace(need, q.device)
+    rc = lib.kda_chunk_fwd_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta),
+                                     _ptr(A_log), _ptr(cu_seqlens), N, T, H, dk, dv, dt,
+                                     _ptr(initial_state), _ptr(final_state), _ptr(o),
+                                     int(segments), _ptr(workspace), workspace.numel(),
+                                     _stream(stream))
+    if rc != KDA_OK:
+        raise KdaError(rc, "kda_chunk_fwd_segmented")
     if check:
         query_status(workspace, stream, raise_on_error=True)
     return o, final_state

@@ -117,6 +117,45 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                          void *stream);
 
 /*
+ * Segment-parallel prefill: kda_chunk_fwd for a few long sequences.  The pages'
+ * KDA context parallelism (dev.to page "Kimi K3 Architecture...", section
+ * "Infrastructure and Training/Inference Mechanics": per-rank state maps merged
+ * by a prefix scan) applied inside one GPU, to segments of each sequence.
+ *
+ * On the tensor-core path (bf16, dk = dv = 128), within each window of chunk
+ * records every sequence's chunks are cut into s = min(segments, chunks)
+ * near-equal consecutive segments.  A first pass walks segment 0 from the
+ * sequence's state (writing its outputs) while every later segment k walks from
+ * [I | 0] with [0 | U~], giving its affine map S_end = M_k S_start + B_k
+ * (M_k is dk x dk: the state's evolution with V = 0).  A scan composes the maps
+ * into each later segment's start state (fp32), and a second pass walks the later
+ * segments from those states, writing their outputs and the final state.  The
+ * sequential depth per window falls from L chunks to about 2 L / s, at the price
+ * of (dk + dv) / dv times the chain work on later segments; it pays off when
+ * sequences x heads leave most SMs idle.  The windows run one after the other on
+ * `stream` alone.  With segments == 1, or off the tensor-core path, this is
+ * kda_chunk_fwd.  Results equal kda_chunk_fwd's up to rounding (the later
+ * segments' start states go through the composed maps).
+ *
+ * Arguments are those of kda_chunk_fwd, plus:
+ *   segments      1 ..= 64
+ *   workspace     >= kda_chunk_fwd_segmented_workspace_size(..., segments) bytes,
+ *                 256-byte aligned (adds num_seqs x H x segments x dk x (dk + 2 dv)
+ *                 fp32 on the tensor-core path)
+ * Errors: those of kda_chunk_fwd; KDA_ERR_INVALID_ARG for segments outside 1 ..= 64.
+ */
+size_t kda_chunk_fwd_segmented_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
+                                              int32_t dk, int32_t dv, int32_t dtype,
+                                              int32_t segments);
+kda_status kda_chunk_fwd_segmented(const void *q, const void *k, const void *v, const void *z,
+                                   const void *beta, const float *A_log,
+                                   const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t H, int32_t dk, int32_t dv,
+                                   int32_t dtype, const float *initial_state, float *final_state,
+                                   void *o, int32_t segments, void *workspace,
+                                   size_t workspace_bytes, void *stream);
+
+/*
  * kda_chunk_fwd with per-kernel timing: identical arguments and results, plus
  * `events`, an array of n_events caller-created cudaEvent_t handles (created
  * with timing enabled).  The call brackets its j-th kernel with events[2j]

@@ -110,6 +110,17 @@ def _chain_shape(N, H):
     return 32 if N * H * 4 <= 2 * sms else 128
 
 
+@pytest.mark.parametrize("z_shift", [-4.0, -6.0])
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 64)])
+def test_long_memory_gates(z_shift, dtype, dk, dv):
+    """Gates near g = 0 keep the state for hundreds of tokens, so every chunk's output leans
+    on the state carried across many chunks (with the default gates it is forgotten within
+    a chunk); an error in the inter-chunk recurrence shows here."""
+    d = inputs.make_prefill([2000, 700, 65], H=4, dk=dk, dv=dv, dtype=dtype, seed=int(-z_shift),
+                            h0_sigma=0.1, z_shift=z_shift, device=DEV)
+    _run_and_score(d, dtype)
+
+
 @pytest.mark.parametrize("lens", [[130, 257], [130, 257, 64, 3] * 3],
                          ids=["few-seqs", "many-seqs"])
 def test_both_chain_shapes(lens):

@@ -308,11 +308,63 @@ def run_ours(args, rank, world, local):
     }
     if not args.no_decode:
         line["decode"] = decode_bench(args, dev, stream, world, pk, pk_src)
+    if not args.no_segmented:
+        line["segmented"] = segmented_bench(dev)
     if not args.no_e2e:
         line["e2e"] = e2e_bench(args, d, dev, stream, world)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(d, args)
     return line
+
+
+# the segment-parallel entry's workload: one long sequence with few heads, where the plain
+# walk keeps only H x 4 SMs busy (name, lengths, heads, segments)
+SEGMENTED = ("prefill_1m_h4", (1 << 20,), 4, 8)
+
+
+def segmented_bench(dev):
+    """kda_chunk_fwd_segmented against kda_chunk_fwd on the same inputs (a long sequence
+    with few heads): CUDA events, L2 flushed between steps, the median of three steps
+    after one untimed call each."""
+    import torch
+
+    from gated_delta_rule_43_gb300 import inputs, kda
+
+    name, lens, H, segs = SEGMENTED
+    d = inputs.make_prefill(list(lens), H=H, dk=128, dv=128, dtype="bf16", seed=6, device=dev)
+    T, N = sum(lens), len(lens)
+    o = torch.empty(T, H, 128, dtype=torch.bfloat16, device=dev)
+    hT = torch.empty(N, H, 128, 128, dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+
+    def run(seg):
+        nbytes = kda.load().kda_chunk_fwd_segmented_workspace_size(T, N, H, 128, 128,
+                                                                   kda.KDA_BF16, seg)
+        ws = kda.alloc_workspace(nbytes, dev)
+
+        def call():
+            kda.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                                    d["cu_seqlens"], None, segments=seg, o=o, final_state=hT,
+                                    workspace=ws)
+        call()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(3):
+            flush.zero_()
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            call()
+            e.record()
+            torch.cuda.synchronize(dev)
+            ts.append(s.elapsed_time(e))
+        kda.query_status(ws, raise_on_error=True)
+        return sorted(ts)[1]
+
+    plain_ms, seg_ms = run(1), run(segs)
+    return {"workload": f"{name}: B=1, H={H}, T={T}, dk=dv=128, bf16, zero initial state",
+            "segments": segs, "plain_ms": plain_ms, "segmented_ms": seg_ms,
+            "plain_tokens_per_s": T / plain_ms * 1e3, "segmented_tokens_per_s": T / seg_ms * 1e3,
+            "speedup": plain_ms / seg_ms}
 
 
 def decode_bench(args, dev, stream, world, pk, pk_src):
@@ -526,6 +578,7 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-segmented", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.warmup < 3:

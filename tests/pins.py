@@ -310,8 +310,37 @@ def pin_score_sums(orc):
             assert abs(sc["ref2"][n, h] - r2) <= 1e-12 * r2
 
 
+def pin_segment_maps(orc):
+    """The final state is affine in the initial one, S_T = M S_0 + B: M is the final state
+    from S_0 = I with v = 0 (the state's evolution without values) and B the final state
+    from S_0 = 0.  The maps of consecutive segments compose into the whole sequence's; this
+    is the algebra the segment-parallel prefill relies on."""
+    rng = np.random.default_rng(12)
+    T, H, dk, dv = 30, 2, 5, 4
+    q, k, v, z, beta, A = _inputs(rng, T, H, dk, dv)
+    h0 = rng.standard_normal((1, H, dk, dv))
+    whole = orc.forward(q, k, v, z, beta, A, [0, T], h0)["state"][0]
+
+    def seg_map(a, b):
+        n = b - a
+        eye = np.broadcast_to(np.eye(dk), (1, H, dk, dk)).copy()
+        M = orc.forward(q[a:b], k[a:b], np.zeros((n, H, dk)), z[a:b], beta[a:b], A, [0, n],
+                        eye)["state"][0]
+        B = orc.forward(q[a:b], k[a:b], v[a:b], z[a:b], beta[a:b], A, [0, n])["state"][0]
+        return M, B
+
+    M, B = seg_map(0, T)
+    _close(np.einsum("hij,hjk->hik", M, h0[0]) + B, whole, 1e-12, "S_T = M S_0 + B")
+    for t in (7, 16, 23):
+        M1, B1 = seg_map(0, t)
+        M2, B2 = seg_map(t, T)
+        s1 = np.einsum("hij,hjk->hik", M1, h0[0]) + B1
+        _close(np.einsum("hij,hjk->hik", M2, s1) + B2, whole, 1e-12, f"composed at {t}")
+
+
 PINS = [pin_gate_closed_forms, pin_gate_bounds, pin_tile_cumsum, pin_softplus_baseline,
         pin_single_step,
         pin_dense_bruteforce, pin_noop, pin_pure_decay, pin_householder, pin_contraction,
         pin_split_resume, pin_varlen_independence, pin_decode_matches_prefill,
-        pin_chunk_algebra, pin_column_blocks, pin_bf16_reader, pin_score_sums]
+        pin_chunk_algebra, pin_column_blocks, pin_bf16_reader, pin_score_sums,
+        pin_segment_maps]

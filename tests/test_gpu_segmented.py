@@ -103,6 +103,29 @@ def test_long_memory_maps(segments):
     assert rel_l2(to_f64(hT), to_f64(s0)) <= TOL["bf16"]
 
 
+def test_nan_decay_is_reported_and_isolated():
+    """A NaN z in the second sequence is reported with its (token, head); the first
+    sequence, cut into segments, still matches the oracle."""
+    import numpy as np
+    from oracle import oracle as orc
+    d = inputs.make_prefill([900, 400], H=2, dk=128, dv=128, dtype="bf16", seed=96,
+                            h0_sigma=0.1, z_shift=-4.0, device=DEV)
+    d["z"][1000, 1, 9] = float("nan")
+    nbytes = kda.load().kda_chunk_fwd_segmented_workspace_size(1300, 2, 2, 128, 128,
+                                                               kda.KDA_BF16, 4)
+    ws = kda.alloc_workspace(nbytes, DEV)
+    o, hT = kda.chunk_fwd_segmented(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                                    d["cu_seqlens"], d["h0"], segments=4, workspace=ws)
+    code, info = kda.query_status(ws)
+    assert code == kda.KDA_ERR_DECAY_RANGE and info == 1000 * 2 + 1
+    h = {n: inputs.host_array(d[n][:900]) for n in ("q", "k", "v", "z", "beta")}
+    ref = orc.forward(h["q"], h["k"], h["v"], h["z"], h["beta"],
+                      d["A_log"].cpu().numpy().astype(np.float64), np.array([0, 900]),
+                      d["h0"][:1].cpu().numpy().astype(np.float64))
+    assert rel_l2(to_f64(o[:900]), ref["o"]) <= TOL["bf16"]
+    assert rel_l2(to_f64(hT[:1]), ref["state"]) <= TOL["bf16"]
+
+
 def test_bad_segment_counts_are_refused():
     d = inputs.make_prefill([100], H=1, dk=128, dv=128, dtype="bf16", seed=94, device=DEV)
     for bad in (0, 65):

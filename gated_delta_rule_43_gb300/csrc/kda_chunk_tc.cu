@@ -746,7 +746,10 @@ __device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float 
 //   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
 //   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
 // D1 is double-buffered in TMEM so that the output rows of chunk c (D1[64:128])
-// are stored by warps 2-3 while warps 0-1 form U of chunk c+1.
+// are stored by warps 2-3 while warps 0-1 form U of chunk c+1.  In the segment-parallel
+// modes (SegArgs) an item is one segment of a sequence's chunks in the window, and a map
+// item walks a 32-column block of [M | B] from [I | 0] (Ut = 0 for the M columns)
+// without storing outputs.
 __global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,

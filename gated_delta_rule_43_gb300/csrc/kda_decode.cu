@@ -7,8 +7,9 @@
 // which is the update of the dev.to page "Kimi K3 Architecture...", section
 // "The Sequence Bottleneck" (state S_t, retention alpha_t, delta strength
 // beta_t) for a single token.  The state is read once and written once: one
-// CTA per (n, h), each thread holding R rows x 4 columns of S in registers
-// between the read and the write, so no column is fetched twice.
+// CTA per (n, h, block of value columns; two 64-column blocks at dv = 128), each
+// thread holding R rows x 4 columns of S in registers between the read and the
+// write, so no column is fetched twice.
 //
 // With a slot index, sequence n reads and writes slot slot_idx[n] of a state
 // pool [P, H, dk, dv] instead of state n (the fixed-size KDA states of the

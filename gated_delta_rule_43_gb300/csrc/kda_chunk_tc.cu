@@ -158,7 +158,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
             const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
-            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st, int ahead,
+            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st,
             const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
             const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ uint8_t smem_raw[];
@@ -213,24 +213,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     const int c = 8 * ch;
     const float alog = A_log[h];
     const float beta_v = tid < L ? __bfloat162float(beta[(t0 + min(tid, C - 1)) * H + h]) : 0.f;
-    // The CTA `ahead` blocks later in launch order starts about one wave after this one:
-    // pull its q, k, z, v rows into L2 now (thread = (tensor, row), two 128-byte lines).
-    {
-        const int64_t lin = (int64_t)blockIdx.y * gridDim.x + blockIdx.x + ahead;
-        int n2 = 0, L2 = 0;
-        int64_t t2 = 0;
-        if (lin < (int64_t)gridDim.x * gridDim.y &&
-            slot_chunk(cu, chunk_off, N, slot0 + prep_slot((int32_t)(lin / gridDim.x), (int32_t)gridDim.y),
-                       n2, t2, L2)) {
-            const int tsel = (tid >> 6) & 3, rr = tid & 63;
-            const __nv_bfloat16 *src = tsel == 0 ? q : tsel == 1 ? k : tsel == 2 ? z : v;
-            if (tid < 256 && rr < L2) {
-                const __nv_bfloat16 *row = src + ((t2 + rr) * H + (int)(lin % gridDim.x)) * (int64_t)DK;
-                prefetch_l2(row);
-                prefetch_l2(row + 64);
-            }
-        }
-    }
     const float expA = expf(alog);
     if (tid < C) BETA[tid] = beta_v;
     __syncthreads();                           // the barriers' initialisation is visible
@@ -1510,7 +1492,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, recs, st, 2 * sm_count, tmap_q, tmap_k, tmap_z, tmap_v);
+            (int32_t)s0, recs, st, tmap_q, tmap_k, tmap_z, tmap_v);
         if (rec) rec->mark(sp);
         if (piped) {
             e = cudaEventRecord(P->prep_done[par], sp);
@@ -1587,7 +1569,7 @@ cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, s>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, records, st, 2 * sm_count, tmap_q, tmap_k, tmap_z, tmap_v);
+            (int32_t)s0, records, st, tmap_q, tmap_k, tmap_z, tmap_v);
         const int64_t pairs = std::min<int64_t>(N, s1 - s0) * H;
         const int64_t items1 = pairs * (c32::NBLK + 2 * c32::NBLK * (segs - 1));
         c32::chain_kernel<<<(unsigned)std::min<int64_t>(items1, sm_count), c32::CHAIN_THREADS,

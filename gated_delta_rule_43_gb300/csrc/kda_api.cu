@@ -129,6 +129,28 @@ ChunkLayout chunk_layout_seg(int64_t T, int32_t N, int32_t H, int32_t dk, int32_
     return L;
 }
 
+// The segment count kda_chunk_fwd picks by itself on the tensor-core path: the largest
+// s <= 16 whose first pass, N H (4 + 8 (s - 1)) 32-column CTAs, still fits one wave of
+// the current device's SMs while the average sequence keeps >= 64 chunks per segment;
+// 1 (the plain schedule) when even s = 2 does not qualify.  Measured: one 1M-token
+// sequence with 4 heads runs in 10.1 ms with 5 segments against 16.0 ms plain; the
+// benchmark workloads (8K with 32 heads, 1M with 16, 64 packed sequences) stay plain.
+int32_t auto_segments(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype) {
+    if (!use_tc(dtype, dk, dv) || N <= 0 || T <= 0) return 1;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 1;
+    const int64_t pairs = (int64_t)N * H;
+    const int64_t chunks = T / ((int64_t)kTcChunk * N);   // whole chunks of the average sequence
+    int32_t best = 1;
+    for (int32_t s = 2; s <= 16; ++s) {
+        if (pairs * (4 + 8 * (s - 1)) > sms || chunks < 64 * (int64_t)s) break;
+        best = s;
+    }
+    return best;
+}
+
 kda_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA; }
 
 // Grids over chunk slots use gridDim.x, which is limited to 2^31 - 1.
@@ -226,7 +248,8 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
     if (total_tokens < 0 || num_seqs < 0 || H <= 0 || !head_ok(dk) || !head_ok(dv) ||
         (dtype != KDA_F32 && dtype != KDA_BF16))
         return 0;
-    return chunk_layout(total_tokens, num_seqs, H, dk, dv, dtype).total;
+    return chunk_layout_seg(total_tokens, num_seqs, H, dk, dv, dtype,
+                            auto_segments(total_tokens, num_seqs, H, dk, dv, dtype)).total;
 }
 
 size_t kda_chunk_fwd_segmented_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
@@ -246,9 +269,14 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
                          int32_t dv, int32_t dtype, const float *initial_state,
                          float *final_state, void *o, void *workspace, size_t workspace_bytes,
                          void *stream) {
+    // the segment-parallel schedule when it pays and the workspace holds it
+    int32_t segs = auto_segments(total_tokens, num_seqs, H, dk, dv, dtype);
+    if (segs > 1 &&
+        workspace_bytes < chunk_layout_seg(total_tokens, num_seqs, H, dk, dv, dtype, segs).total)
+        segs = 1;
     return chunk_fwd_impl(q, k, v, z, beta, A_log, cu_seqlens, num_seqs, total_tokens, H, dk, dv,
                           dtype, initial_state, final_state, o, workspace, workspace_bytes, stream,
-                          nullptr);
+                          nullptr, segs);
 }
 
 kda_status kda_chunk_fwd_segmented(const void *q, const void *k, const void *v, const void *z,

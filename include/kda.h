@@ -67,7 +67,9 @@ const char *kda_status_string(int32_t status);
  * workspace holds the status word, the chunk plan of the packed sequences
  * and the intermediates of the chunked form; its contents need no
  * initialisation and are overwritten by every call.  Returns 0 for
- * arguments kda_chunk_fwd would reject.
+ * arguments kda_chunk_fwd would reject.  On the tensor-core path the size
+ * includes the segment-parallel schedule's buffers when kda_chunk_fwd would pick
+ * that schedule on the current device (see kda_chunk_fwd).
  */
 size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H,
                                     int32_t dk, int32_t dv, int32_t dtype);
@@ -84,7 +86,12 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
  * first token; the intra-chunk part runs as dense products over 16-token
  * tiles (the chunkwise-parallel form of the dev.to page, section "The
  * Sequence Bottleneck").  The result equals the token-by-token recurrence
- * up to rounding.
+ * up to rounding.  On the tensor-core path, when a few long sequences would
+ * leave most SMs idle (num_seqs x H x (4 + 8 (s - 1)) 32-column chain CTAs for s
+ * segments fit one wave of the device's SMs, with >= 64 chunks per segment of the
+ * average sequence, s >= 2), the call runs the segment-parallel schedule of
+ * kda_chunk_fwd_segmented with the largest such s <= 16, provided the workspace
+ * holds its buffers (the size query includes them); otherwise the plain schedule.
  *
  * Work is enqueued on `stream` and returns without synchronising.  On the
  * tensor-core path (bf16, dk = dv = 128) a problem with more than one window
@@ -133,9 +140,10 @@ kda_status kda_chunk_fwd(const void *q, const void *k, const void *v, const void
  * sequential depth per window falls from L chunks to about 2 L / s, at the price
  * of (dk + dv) / dv times the chain work on later segments; it pays off when
  * sequences x heads leave most SMs idle.  The windows run one after the other on
- * `stream` alone.  With segments == 1, or off the tensor-core path, this is
- * kda_chunk_fwd.  Results equal kda_chunk_fwd's up to rounding (the later
- * segments' start states go through the composed maps).
+ * `stream` alone.  segments == 1, or any call off the tensor-core path, is the
+ * plain schedule.  Results equal the plain schedule's up to rounding (the later
+ * segments' start states go through the composed maps).  kda_chunk_fwd picks this
+ * schedule by itself for the shapes where it pays; this entry fixes the count.
  *
  * Arguments are those of kda_chunk_fwd, plus:
  *   segments      1 ..= 64

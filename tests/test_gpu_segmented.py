@@ -126,6 +126,44 @@ def test_nan_decay_is_reported_and_isolated():
     assert rel_l2(to_f64(hT[:1]), ref["state"]) <= TOL["bf16"]
 
 
+def _auto_segments(T, N, H):
+    """The count kda_chunk_fwd picks by itself (include/kda.h): the largest s <= 16 whose
+    first pass fits one wave of 32-column CTAs, with >= 64 chunks per segment."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    chunks = T // (64 * N)
+    best = 1
+    for s in range(2, 17):
+        if N * H * (4 + 8 * (s - 1)) > sms or chunks < 64 * s:
+            break
+        best = s
+    return best
+
+
+def test_plain_call_picks_segments_for_few_long_sequences():
+    T, H = 300_000, 2
+    segs = _auto_segments(T, 1, H)
+    assert segs >= 2
+    d = inputs.make_prefill([T], H=H, dk=128, dv=128, dtype="bf16", seed=97, h0_sigma=0.1,
+                            z_shift=-6.0, device=DEV)
+    o, hT = gpu_prefill(d)
+    o_s, hT_s = _seg(d, segs)
+    assert torch.equal(o, o_s) and torch.equal(hT, hT_s)   # the same schedule
+    _score(d, o, hT, heads=[0])
+    # a workspace sized for the plain schedule makes the call fall back to it
+    nplain = kda.load().kda_chunk_fwd_segmented_workspace_size(T, 1, H, 128, 128,
+                                                               kda.KDA_BF16, 1)
+    ws = kda.alloc_workspace(nplain, DEV)
+    o1, h1 = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                           d["cu_seqlens"], d["h0"], workspace=ws, check=True)
+    o_p, h_p = _seg(d, 1)
+    assert torch.equal(o1, o_p) and torch.equal(h1, h_p)
+
+
+def test_benchmark_shapes_stay_plain():
+    for T, N, H in ((8192, 1, 32), (1 << 20, 1, 16), (158_000, 64, 32)):
+        assert _auto_segments(T, N, H) == 1, (T, N, H)
+
+
 def test_bad_segment_counts_are_refused():
     d = inputs.make_prefill([100], H=1, dk=128, dv=128, dtype="bf16", seed=94, device=DEV)
     for bad in (0, 65):

@@ -84,8 +84,7 @@ constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
 constexpr uint32_t P_ZT = 47104;        // (until pass A) z tile, TMA, [2][64][128 B] swizzled
 constexpr uint32_t P_KT = 63488;        // (until the table pass) k tile, likewise
 constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewise
-constexpr uint32_t P_NS = 1024;         // (solve) fp32 N_ab blocks [6][16][16] over the dead tables
-constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], before N
+constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], over the dead tables
 constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
 constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
 constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, fp32 [4][64][32]
@@ -98,7 +97,7 @@ static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "so
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
 static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
                   P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
-static_assert(P_NS + 6 * 256 * 4 <= P_BETA && P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
+static_assert(P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
                   P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
               "solve / epilogue staging overlaps live data");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
@@ -439,28 +438,34 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // with the Q*Gam staging, whose bulk copy is given until the N^3 step to finish; it is
     // written there: zero blocks above the diagonal in the N^3 step, the other blocks in
     // the last step of the solve.
-    float *NS = reinterpret_cast<float *>(sm + P_NS);   // N_ab blocks [pair][16][16]
     uint8_t *TBI = sm + P_TB;
-    if (tid < 64) {  // diagonal blocks T_aa = (I + A_aa)^-1: thread (block tb, column j)
-        const int tb = tid >> 4, j = tid & 15;
-        float tcol[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float s = (i == j) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) s -= AS[(16 * tb + i) * LDA + 16 * tb + m] * tcol[m];
-            tcol[i] = s;   // zero above the diagonal
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) TS[(16 * tb + i) * LDA + 16 * tb + j] = tcol[i];
-    }
-    if (tid == 0) bulk_wait_read_all();   // the P staging (under the N blocks) is free
-    __syncthreads();
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
-    // The diagonal blocks of T hold explicit zeros above the diagonal, so every product
-    // below runs over all 16 terms (fixed trip counts, fully unrolled).
     auto pair_a = [](int pr) { return pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3); };
     auto pair_b = [](int pr) { return pr < 3 ? pr : (pr == 4 ? 1 : 0); };
+    // One step for D^-1 and N: forward substitution down a 16-row column through
+    // (I + A_aa), 64 columns e_j (giving T_aa = (I + A_aa)^-1 on the diagonal of TS) and
+    // 96 columns of A_ab (giving N_ab = T_aa A_ab in block (a, b) of TS, which T itself
+    // never uses: its off-diagonal blocks go straight to the T diag(b) image).
+    if (tid < 64 + 96) {
+        const bool diag = tid < 64;
+        const int pr = diag ? 0 : (tid - 64) >> 4;
+        const int a2 = diag ? tid >> 4 : pair_a(pr);
+        const int b = diag ? a2 : pair_b(pr);
+        const int j = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float s = diag ? ((i == j) ? 1.f : 0.f) : AS[(16 * a2 + i) * LDA + 16 * b + j];
+#pragma unroll
+            for (int m = 0; m < i; ++m) s -= AS[(16 * a2 + i) * LDA + 16 * a2 + m] * x[m];
+            x[i] = s;   // T_aa: zero above the diagonal
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) TS[(16 * a2 + i) * LDA + 16 * b + j] = x[i];
+    }
+    __syncthreads();
+    // The diagonal blocks of T hold explicit zeros above the diagonal, so every product
+    // below runs over all 16 terms (fixed trip counts, fully unrolled).
     // dst += X[16 x 16 block rows] (row i) times Y (16 x 4 column group)
     auto acc16 = [](float4 &x, const float *xrow, const float *ycol, int ystride) {
 #pragma unroll
@@ -470,34 +475,21 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             x.x += xv * y.x; x.y += xv * y.y; x.z += xv * y.z; x.w += xv * y.w;
         }
     };
-    // N_ab = T_aa A_ab
-#pragma unroll
-    for (int w = 0; w < SOLVE_W; ++w) {
-        const int task = tid + w * PREP_THREADS;   // 384 tasks: (pair, row i, 4-column group)
-        if (task < 384) {
-            const int pr = task >> 6, i = (task >> 2) & 15, jq = task & 3;
-            const int a2 = pair_a(pr), b = pair_b(pr);
-            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-            acc16(x, TS + (16 * a2 + i) * LDA + 16 * a2, AS + (16 * a2) * LDA + 16 * b + 4 * jq, LDA);
-            *reinterpret_cast<float4 *>(NS + pr * 256 + i * 16 + 4 * jq) = x;
-        }
-    }
-    __syncthreads();
     float *XS = reinterpret_cast<float *>(sm + P_XS);   // [0] N2_20 [1] N2_31 [2] N2_30 [3] N3_30
-    // N_ab row i, and the 4-column group jq of N_ab, for pair numbers p
-    auto nrow = [&](int p, int i) { return NS + p * 256 + i * 16; };
-    auto ncol = [&](int p, int jq) { return NS + p * 256 + 4 * jq; };
+    // N_ab row i, and the 4-column group jq of N_ab (row stride LDA), for pair numbers p
+    auto nrow = [&](int p, int i) { return TS + (16 * pair_a(p) + i) * LDA + 16 * pair_b(p); };
+    auto ncol = [&](int p, int jq) { return TS + (16 * pair_a(p)) * LDA + 16 * pair_b(p) + 4 * jq; };
     if (tid < 192) {
         // N^2 blocks: (2,0) = N21 N10, (3,1) = N32 N21, (3,0) = N31 N10 + N32 N20 (warp-uniform q)
         const int q = tid >> 6, i = (tid >> 2) & 15, jq = tid & 3;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (q == 0) {
-            acc16(x, nrow(1, i), ncol(0, jq), 16);
+            acc16(x, nrow(1, i), ncol(0, jq), LDA);
         } else if (q == 1) {
-            acc16(x, nrow(2, i), ncol(1, jq), 16);
+            acc16(x, nrow(2, i), ncol(1, jq), LDA);
         } else {
-            acc16(x, nrow(4, i), ncol(0, jq), 16);
-            acc16(x, nrow(2, i), ncol(3, jq), 16);
+            acc16(x, nrow(4, i), ncol(0, jq), LDA);
+            acc16(x, nrow(2, i), ncol(3, jq), LDA);
         }
         *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
     }

@@ -1,17 +1,22 @@
 #!/usr/bin/env python3
 """Benchmark of the KDA hot path on GB300: chunked prefill tokens/s and decode state GB/s.
 
-Default run (N=1): the prefill_8k workload (one sequence, T=8192, H=32,
-dk=dv=128, bf16 inputs, fp32 final state) through kda_chunk_fwd -- one step is
-one full chunked forward (gate, intra-chunk transform, state recurrence,
-output).  The same line carries the decode workload (256 sequences x 1 token,
+Default run (N=1): the headline is the prefill_1m workload -- one sequence of
+T = 1,048,576 tokens, H=16, dk=dv=128, bf16 inputs, fp32 state carried over
+the whole length and emitted -- through kda_chunk_fwd; one step is one full
+chunked forward (gate, intra-chunk transform, state recurrence, output).  The
+same line carries the other workloads measured the same way (prefill_8k: one
+8192-token sequence with 32 heads; varlen_64: 64 packed sequences of 512-4096
+tokens with initial states), the decode workload (256 sequences x 1 token,
 H=32, 128 consecutive in-place steps on a 512 MiB fp32 state) through
-kda_decode_step, the roofline of the dominant kernel, the end-to-end number
-with host buffers, the CPU oracle timed on the host cores, and the SM clocks
-seen during the timed region.
+kda_decode_step, the roofline of each workload's dominant kernel, the
+end-to-end number with host buffers, the CPU oracle timed on the host cores,
+and the SM clocks seen during the timed region.
 
-With --impl reference the fp64 CPU oracle runs the same workload on the host
-cores (a bounded sample of tokens per step) and prints the same JSON line.
+With --impl reference the fp64 CPU oracle runs the headline workload (the
+same seeded inputs, drawn by the same generator on the same device) on the
+host cores, a bounded prefix of the tokens per step, and prints the same JSON
+line.
 
 Multi-GPU (torchrun, one rank per GPU): every rank runs its own replica of the
 workload (the (sequence, head) units are independent; no collective is on the
@@ -34,30 +39,40 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s and decode state GB/s per GB300; % of roofline"
-PREFILL = "prefill_8k"
+HEADLINE = "prefill_1m"
+EXTRA_PREFILL = ("prefill_8k", "varlen_64")
 DECODE = "decode_256"
 L2_BYTES = 129 * 1024 * 1024
 FLUSH_BYTES = 256 * 1024 * 1024
 
 
-def profiled_traffic(md_name: str):
-    """DRAM bytes per launch from a committed ncu summary under profiles/, or None when
-    the kernel sources it names have changed since the capture."""
+def profiled_traffic(md_name: str, units_per_launch: float | None = None):
+    """DRAM bytes per launch from a committed ncu summary under profiles/, or None when the
+    summary is absent or the kernel sources it names have changed since the capture.  A
+    summary taken on a smaller case of the same kernel gives bytes per token-head
+    (`traffic_bytes_per_token_head`), scaled here by the token-heads one launch processes."""
     import hashlib
+    keys = ("traffic_bytes_per_launch", "traffic_bytes_per_token_head", "source_sha256_16",
+            "sources")
     try:
         text = open(os.path.join(ROOT, "profiles", md_name)).read()
         fields = dict(line.strip().split(": ", 1) for line in text.splitlines()
-                      if line.strip().split(": ", 1)[0] in
-                      ("traffic_bytes_per_launch", "source_sha256_16", "sources"))
+                      if line.strip().split(": ", 1)[0] in keys)
         h = hashlib.sha256()
         for f in fields["sources"].split():
             with open(os.path.join(ROOT, f), "rb") as fh:
                 h.update(fh.read())
         if h.hexdigest()[:16] != fields["source_sha256_16"]:
             return None
-        return int(fields["traffic_bytes_per_launch"])
+        if "traffic_bytes_per_launch" in fields:
+            return int(fields["traffic_bytes_per_launch"])
+        if units_per_launch is None:
+            return None
+        return int(float(fields["traffic_bytes_per_token_head"]) * units_per_launch)
     except (OSError, KeyError, ValueError):
         return None
+
+
 # fallbacks only when the measured peaks file is absent
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -198,17 +213,36 @@ def aggregate(per_rank_units: float, elapsed_s: float, world: int) -> tuple[floa
 
 # ----------------------------------------------------------------------------- GPU arm
 
-def run_ours(args, rank, world, local):
+def workload_config(name: str, world: int = 1) -> dict:
+    """The `config` object of a prefill workload's line (identical in both arms)."""
+    from gated_delta_rule_43_gb300 import inputs
+
+    w = inputs.WORKLOADS[name]
+    if w.seqlens and w.seqlens[0] == "uniform":
+        _, cnt, lo, hi = w.seqlens
+        shape = f"{cnt} packed sequences, lengths uniform in [{lo}, {hi}]"
+    else:
+        shape = f"B={len(w.seqlens)}, T={sum(w.seqlens)}"
+    h0 = (f"initial state N(0, {w.h0_sigma ** 2:g}) fp32" if w.h0_sigma > 0
+          else "zero initial state")
+    return {"workload": f"{name}: {shape}, H={w.H}, dk={w.dk}, dv={w.dv}, {w.dtype} "
+                        f"q/k/v/z/beta, {h0}, fp32 final state emitted",
+            "heads": w.H, "dk": w.dk, "dv": w.dv, "seed": w.seed,
+            "inputs": "seeded synthetic (gated_delta_rule_43_gb300/inputs.py), drawn on the GPU",
+            "l2": "flushed between timed steps (256 MiB write outside the events); the "
+                  "1M-token inputs (17 GB) are also far larger than L2",
+            "parallelism": f"replicas x{world}"}
+
+
+def prefill_leg(name, dev, stream, K, warmup, world, pk, pk_src, clock=False, keep=False):
+    """One prefill workload through kda_chunk_fwd: K timed whole calls (L2 flushed between
+    them), then K calls through kda_chunk_fwd_profiled for per-kernel times on the streams
+    the kernels run on.  Returns (result dict, inputs or None)."""
     import torch
 
-    from gated_delta_rule_43_gb300 import _build, inputs, kda
+    from gated_delta_rule_43_gb300 import inputs, kda
 
-    _build.build()
-    kda.load()
-    dev = torch.device("cuda", local)
-    stream = torch.cuda.current_stream(dev)
-    pk, pk_src = peaks()
-    w = inputs.WORKLOADS[PREFILL]
+    w = inputs.WORKLOADS[name]
     d = inputs.make_workload(w, device=dev)
     T = sum(d["seqlens"])
     N = len(d["seqlens"])
@@ -222,12 +256,11 @@ def run_ours(args, rank, world, local):
         kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
                       d["h0"], o=o, final_state=hT, workspace=ws, stream=stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     kda.query_status(ws, stream, raise_on_error=True)
 
-    K = args.steps
-    NEV = 512
+    NEV = 1024
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     kev = [[torch.cuda.Event(enable_timing=True) for _ in range(NEV)] for _ in range(K)]
@@ -237,19 +270,22 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     barrier(world)
     torch.cuda.synchronize(dev)
-    # the headline: whole calls of the public entry, timed on the caller's stream
-    with ClockSampler(local) as clk:
-        for i in range(K):
-            flush.zero_()                       # evict L2 between timed steps
-            starts[i].record(stream)
-            step()
-            ends[i].record(stream)
-        torch.cuda.synchronize(dev)
+    clk = ClockSampler(dev.index or 0) if clock else None
+    if clk:
+        clk.__enter__()
+    # whole calls of the public entry, timed on the caller's stream
+    for i in range(K):
+        flush.zero_()                       # evict L2 between timed steps
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize(dev)
+    if clk:
+        clk.__exit__(None, None, None)
     barrier(world)
     kda.query_status(ws, stream, raise_on_error=True)
     step_ms = [s_.elapsed_time(e_) for s_, e_ in zip(starts, ends)]
-    elapsed = sum(step_ms) / 1e3
-    value, tmax = aggregate(T * K, elapsed, world)
+    value, tmax = aggregate(T * K, sum(step_ms) / 1e3, world)
     # per-kernel times: the same K calls through the profiled entry, which brackets
     # every kernel with two events on the stream that kernel runs on
     used = []
@@ -269,7 +305,6 @@ def run_ours(args, rank, world, local):
     totals = {nm: sum(v_) / K for nm, v_ in per_kernel.items()}       # ms per step
     launches = {nm: names.count(nm) for nm in totals}
     dom = max(totals, key=totals.get)
-    launches_per_step = len(names)
     algo_bytes = prefill_bytes(d["seqlens"], H, dk, dv, 2, d["h0"] is not None, True)
     step_s = statistics.mean(step_ms) / 1e3
     dom_s = totals[dom] / 1e3
@@ -278,42 +313,77 @@ def run_ours(args, rank, world, local):
     tflops = flops / step_s / 1e12
     hbm_peak = pk.get("hbm_gbs", FALLBACK["hbm_gbs"])
     tc_peak = pk.get("bf16_tflops", FALLBACK["bf16_tflops"])
-
-    line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": tmax * 1e3 / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{PREFILL}: B=1, H=32, T=8192, dk=dv=128, bf16 q/k/v/z/beta, "
-                               "zero initial state, fp32 final state emitted",
-                   "tokens_per_step": T, "heads": H, "dk": dk, "dv": dv,
-                   "l2": "flushed between timed steps (256 MiB write outside the events)",
-                   "parallelism": f"replicas x{world}"},
+    units_per_launch = T * H / launches[dom]
+    res = {
+        "value": value, "unit": "tokens/s", "ms_per_step": tmax * 1e3 / K,
+        "ms_per_step_all": step_ms, "steps": K, "tokens_per_step": T,
+        "config": workload_config(name, world),
         "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved_gbs / hbm_peak,
-                     "traffic": (profiled_traffic(f"{dom}_prefill_8k.md")
-                                 if dom in ("prep_kernel", "chain_kernel") else None),
+                     "traffic": profiled_traffic(f"{dom}_{name}.md", units_per_launch),
                      "kernel": dom, "peak_source": pk_src,
                      "algorithmic_bytes_per_launch": algo_bytes / launches[dom],
+                     "token_heads_per_launch": units_per_launch,
                      "launches_per_step": launches[dom],
                      "avg_launch_us": dom_s / launches[dom] * 1e6,
                      "kernel_ms_per_step": totals,
+                     "kernel_launches_per_step": launches,
                      "step": {"achieved_gbs": algo_bytes / step_s / 1e9,
                               "frac": algo_bytes / step_s / 1e9 / hbm_peak,
                               "algorithmic_bytes": algo_bytes},
                      "tensor": {"achieved_tflops": tflops, "peak_tflops": tc_peak,
                                 "frac": tflops / tc_peak, "flops_per_step": flops,
                                 "convention": "6 dk dv + 64 (3 dk + 2 dv) per token-head"}},
-        "gpu_launches": launches_per_step * K,
-        "clocks": clk.summary(),
+        "gpu_launches": len(names) * K,
     }
-    if not args.no_decode:
-        line["decode"] = decode_bench(args, dev, stream, world, pk, pk_src)
-    if not args.no_segmented:
-        line["segmented"] = segmented_bench(dev)
+    if clk:
+        res["clocks"] = clk.summary()
+    del ws, o, hT, flush
+    if not keep:
+        del d
+        torch.cuda.empty_cache()
+        return res, None
+    return res, d
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    from gated_delta_rule_43_gb300 import _build, kda
+
+    _build.build()
+    kda.load()
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk, pk_src = peaks()
+    head, d = prefill_leg(HEADLINE, dev, stream, args.steps, args.warmup, world, pk, pk_src,
+                          clock=True, keep=True)
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": head["config"], "roofline": head["roofline"],
+        "gpu_launches": head["gpu_launches"], "clocks": head["clocks"],
+        "ms_per_step_all": head["ms_per_step_all"],
+    }
     if not args.no_e2e:
         line["e2e"] = e2e_bench(args, d, dev, stream, world)
+    sample = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(d, args)
+        sample = host_prefix(d, CPU_SAMPLE_MAX)
+    del d
+    torch.cuda.empty_cache()
+    if not args.headline_only:
+        line["workloads"] = {}
+        for name in EXTRA_PREFILL:
+            res, _ = prefill_leg(name, dev, stream, args.steps, args.warmup, world, pk, pk_src)
+            line["workloads"][name] = res
+        if not args.no_decode:
+            line["decode"] = decode_bench(args, dev, stream, world, pk, pk_src)
+        if not args.no_segmented:
+            line["segmented"] = segmented_bench(dev)
+    if sample is not None:
+        line["cpu_baseline"] = cpu_baseline(sample, args)
     return line
 
 
@@ -428,7 +498,10 @@ def e2e_bench(args, d, dev, stream, world):
     from gated_delta_rule_43_gb300 import kda
 
     names = ("q", "k", "v", "z", "beta", "A_log", "cu_seqlens")
-    host = {n: d[n].cpu().pin_memory() for n in names}
+    host = {}
+    for n in names:
+        host[n] = torch.empty(d[n].shape, dtype=d[n].dtype, pin_memory=True)
+        host[n].copy_(d[n])
     T, H, dv = d["v"].shape
     N = d["cu_seqlens"].numel() - 1
     dk = d["q"].shape[2]
@@ -497,70 +570,89 @@ def e2e_bench(args, d, dev, stream, world):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_rate(d, target_s: float, nthreads: int = 0):
-    """Time the fp64 oracle on a prefix sample of the prefill workload sized to ~target_s.
+# tokens of the headline workload copied to the host for the oracle's timed sample
+CPU_SAMPLE_MAX = 1 << 16
 
-    Returns (tokens/s, sample description, threads)."""
+
+def host_prefix(d, tmax: int) -> dict:
+    """Host arrays (exact storage precision) of the first tmax tokens of a one-sequence
+    prefill input, all heads; the oracle's timed sample is a prefix of these."""
     import numpy as np
 
     from gated_delta_rule_43_gb300 import inputs
-    from oracle import oracle as orc
 
     T = sum(d["seqlens"])
-    arrs = {n: inputs.host_array(d[n]) for n in ("q", "k", "v", "z", "beta")}
-    A = d["A_log"].cpu().numpy().astype(np.float64)
+    t = min(T, tmax)
+    out = {n: inputs.host_array(d[n][:t]) for n in ("q", "k", "v", "z", "beta")}
+    out["A_log"] = d["A_log"].cpu().numpy().astype(np.float64)
+    out["T"] = T
+    out["H"] = d["q"].shape[1]
+    return out
+
+
+def oracle_sample_rate(hp, target_s: float, nthreads: int = 0):
+    """Time the fp64 oracle on a prefix of the headline workload sized to ~target_s of
+    host work.  Returns (tokens/s, prefix length, threads)."""
+    from oracle import oracle as orc
+
+    avail = hp["q"].shape[0]
 
     def run(t):
         t0 = time.perf_counter()
-        orc.forward(arrs["q"][:t], arrs["k"][:t], arrs["v"][:t], arrs["z"][:t],
-                    arrs["beta"][:t], A, [0, t], None, want_o=True, want_state=True,
-                    nthreads=nthreads)
+        orc.forward(hp["q"][:t], hp["k"][:t], hp["v"][:t], hp["z"][:t], hp["beta"][:t],
+                    hp["A_log"], [0, t], None, want_o=True, want_state=True, nthreads=nthreads)
         return time.perf_counter() - t0
 
-    probe = min(T, 128)
+    probe = min(avail, 128)
     dt = run(probe)
-    t_s = int(min(T, max(probe, probe * target_s / max(dt, 1e-6))))
+    t_s = int(min(avail, max(probe, probe * target_s / max(dt, 1e-6))))
     dt = run(t_s)
     return t_s / dt, t_s, orc.threads() if nthreads <= 0 else nthreads
 
 
-def cpu_baseline(d, args):
-    rate, t_s, thr = oracle_sample_rate(d, args.cpu_seconds)
-    T = sum(d["seqlens"])
+def cpu_baseline(hp, args):
+    rate, t_s, thr = oracle_sample_rate(hp, args.cpu_seconds)
     return {"value": rate, "unit": "tokens/s", "cores": thr, "kind": "oracle",
-            "sample": f"first {t_s} of {T} tokens of {PREFILL}, all 32 heads, fp64 sequential "
-                      f"recurrence (C, OpenMP over head x column-block units)"}
+            "sample": f"first {t_s} of {hp['T']} tokens of {HEADLINE}, all {hp['H']} heads, "
+                      "fp64 sequential recurrence (C, OpenMP over head x column-block units), "
+                      "the same inputs the GPU arm ran"}
 
 
 def run_reference(args, rank, world):
-    """--impl reference: the fp64 oracle on the host cores, bounded sample per step."""
+    """--impl reference: the fp64 oracle on the host cores, a bounded prefix of the headline
+    workload per step.  The inputs are drawn exactly as the GPU arm draws them (the same
+    seeded generator on the GPU, then copied to the host), so both arms see the same values;
+    without a GPU they are drawn on the host (same distributions, other values)."""
     import torch
 
     from gated_delta_rule_43_gb300 import inputs
 
     if rank != 0:
         return None
-    w = inputs.WORKLOADS[PREFILL]
-    d = inputs.make_workload(w, device="cpu")
+    on_gpu = torch.cuda.is_available()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))) if on_gpu else "cpu"
+    d = inputs.make_workload(inputs.WORKLOADS[HEADLINE], device=dev)
+    hp = host_prefix(d, CPU_SAMPLE_MAX)
+    del d
+    if on_gpu:
+        torch.cuda.empty_cache()
     per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
-    rate, t_s, thr = oracle_sample_rate(d, per_step)
-    rates = []
     for _ in range(args.warmup):
-        oracle_sample_rate(d, per_step)
+        oracle_sample_rate(hp, per_step)
+    rates = []
     for _ in range(args.steps):
-        r, t_s, thr = oracle_sample_rate(d, per_step)
+        r, t_s, thr = oracle_sample_rate(hp, per_step)
         rates.append(r)
     value = statistics.mean(rates)
-    T = sum(d["seqlens"])
-    sample = (f"first {t_s} of {T} tokens of {PREFILL} per step, all 32 heads, fp64 "
-              "sequential recurrence on the host cores")
-    del torch
+    sample = (f"first {t_s} of {hp['T']} tokens of {HEADLINE} per step, all {hp['H']} heads, "
+              "fp64 sequential recurrence on the host cores; inputs drawn "
+              + ("on the GPU with the GPU arm's generator (identical values)" if on_gpu else
+                 "on the host (same recipe and seed, host generator: other values)"))
     return {"metric": METRIC, "impl": "reference", "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": t_s / value * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{PREFILL}: B=1, H=32, T=8192, dk=dv=128, bf16 inputs "
-                                   "widened to fp64", "parallelism": "host cores"},
+            "config": workload_config(HEADLINE, world),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -580,6 +672,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-segmented", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time the headline workload (and e2e / CPU baseline) only")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

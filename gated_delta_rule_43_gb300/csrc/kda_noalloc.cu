@@ -11,16 +11,15 @@
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
 // library holds KDA_NOALLOC_SCRATCH_BYTES of it until the process exits.
-// Host code cannot use its name as a device address, so the first call on
-// each device looks the address up with cudaGetSymbolAddress (with that
-// device current) and caches it; that first call should therefore happen
-// before any stream capture.  All calls share the one array: calls whose work
+// Host code cannot use its name as a device address, so every call looks the
+// address up with cudaGetSymbolAddress on the current device (no allocation, and no
+// cached pointer that a cudaDeviceReset could leave stale); the first call on a device
+// also loads the library's device code there, so it should happen before any stream
+// capture.  All calls share the one array: calls whose work
 // overlaps on the GPU (different streams, or different host threads without
 // ordering) race on it and must be serialised by the caller.  Nothing in the
 // array has to start at zero: the status word is cleared by every call and
 // every other byte read by a kernel is written earlier in the same call.
-#include <mutex>
-
 #include "kda_common.cuh"
 
 namespace kda {
@@ -48,24 +47,12 @@ namespace {
 
 static __device__ __align__(256) uint8_t g_noalloc_scratch[KDA_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_setup_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_noalloc_scratch on the current device (looked up once per device).
+// Device address of g_noalloc_scratch on the current device.
 cudaError_t scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_ptr[dev] = p;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = p;
     return cudaSuccess;
 }
 
@@ -74,7 +61,6 @@ inline bool al(const void *p, size_t a) { return ((uintptr_t)p % a) == 0; }
 inline bool head_ok(int32_t d) { return d == 32 || d == 64 || d == 128; }
 
 constexpr int kChunk = 64;                    // tensor-core chunk length
-constexpr size_t kL2Window = 80u << 20;       // same L2 budget as kda_chunk_fwd
 
 }  // namespace
 
@@ -98,10 +84,12 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
         if (!al(p, 16)) return KDA_ERR_INVALID_ARG;
     if (o && (o == q || o == k || o == v || o == z || o == beta)) return KDA_ERR_INVALID_ARG;
     if ((total_tokens + kChunk - 1) / kChunk + num_seqs > 0x7fffffffLL) return KDA_ERR_INVALID_ARG;
-    if (total_tokens >= ((int64_t)1 << 31)) return KDA_ERR_INVALID_ARG;   // 32-bit tile coordinates
-
-    // Scratch layout inside the fixed array; reject what does not fit.
     const bool tc = dtype == KDA_BF16 && dk == 128 && dv == 128;
+    // token coordinates of the tensor-core path's tile loads are 32-bit
+    if (tc && total_tokens >= ((int64_t)1 << 31)) return KDA_ERR_INVALID_ARG;
+
+    // Scratch layout inside the fixed array; reject what does not fit.  The window of
+    // chunk records is whatever the array has left after the plan and the running state.
     const size_t plan_off = kHeaderBytes;
     const size_t plan_bytes = up(sizeof(int32_t) * ((size_t)num_seqs + 1), 1024);
     size_t state_off = plan_off + plan_bytes, state_bytes = 0, rec_off = state_off;
@@ -112,11 +100,9 @@ extern "C" kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const 
         if (rec_off > KDA_NOALLOC_SCRATCH_BYTES) return KDA_ERR_INVALID_ARG;
         const size_t rec = tc_record_bytes() * (size_t)H;
         slots = chunk_slots(total_tokens, num_seqs, kChunk);
-        int64_t fit = (int64_t)((KDA_NOALLOC_SCRATCH_BYTES - rec_off) / rec);
-        const int64_t l2 = (int64_t)(kL2Window / rec) > 0 ? (int64_t)(kL2Window / rec) : 1;
+        const int64_t fit = (int64_t)((KDA_NOALLOC_SCRATCH_BYTES - rec_off) / rec);
         if (fit < 1 && slots > 0) return KDA_ERR_INVALID_ARG;
         window = slots < fit ? slots : fit;
-        if (window > l2) window = l2;
     } else if (plan_off + plan_bytes > KDA_NOALLOC_SCRATCH_BYTES) {
         return KDA_ERR_INVALID_ARG;
     }

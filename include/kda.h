@@ -216,9 +216,13 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
  * problems are rejected with KDA_ERR_INVALID_ARG before anything is launched.
  * Fewer records fit than in a caller-sized workspace, so long inputs run in
  * more, smaller windows.
- * Set-up: the first call on each device looks up the array's device address
- * (with that device current) and caches it; make that first call before any
- * stream capture.
+ * On the CUDA-core path (fp32, or other head sizes) only the status word and
+ * the chunk plan live in the array.
+ * Set-up: every call looks up the array's device address on the current
+ * device with cudaGetSymbolAddress (no allocation, nothing cached, so the
+ * library stays usable after a cudaDeviceReset); the first call on a device
+ * also loads the library's device code there, so make it before any stream
+ * capture.
  * Concurrency: every call uses the same array, which keeps the previous
  * call's contents (each call clears what it needs).  Calls whose work can
  * overlap on the GPU -- on different streams, or from threads that do not

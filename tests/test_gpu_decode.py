@@ -5,32 +5,42 @@ import torch
 
 from gated_delta_rule_43_gb300 import inputs, kda
 from oracle import oracle as orc
-from tests.gpu_util import TOL, gpu_prefill, rel_l2, to_f64
+from tests.gpu_util import TOL, gpu_prefill, oracle_prefill, rel_l2, to_f64
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-def _decode_and_score(N, H, dk, dv, dtype, steps, seqs=None, seed=0):
+def _decode_and_score(N, H, dk, dv, dtype, steps, seed=0):
+    """`steps` in-place decode steps of N sequences against the fp64 oracle: rel-L2 of the
+    outputs of every step (concatenated) and of the state after the last step, both over
+    the whole tensor; the worst single (sequence, head) within three times the tolerance."""
     ds = inputs.DecodeStream(N, H, dk, dv, dtype, seed=seed, h0_sigma=0.1, device=DEV)
     state = ds.state0.clone()
-    sel = list(range(N)) if seqs is None else list(seqs)
-    sel_t = torch.as_tensor(sel, device=DEV)
-    ref_state = state.index_select(0, sel_t).cpu().numpy().astype(np.float64)
+    ref_state = state.cpu().numpy().astype(np.float64)
     A = ds.A_log.cpu().numpy().astype(np.float64)
-    outs, refs = [], []
+    e2 = np.zeros((N, H))
+    r2 = np.zeros((N, H))
     for _ in range(steps):
         x = ds.step()
         o = kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, state)
-        outs.append(to_f64(o.index_select(0, sel_t)))
-        h = {k: inputs.host_array(x[k].index_select(0, sel_t)) for k in x}
-        refs.append(orc.decode(h["q"], h["k"], h["v"], h["z"], h["beta"], A, ref_state))
+        h = {k: inputs.host_array(x[k]) for k in x}
+        ref = orc.decode(h["q"], h["k"], h["v"], h["z"], h["beta"], A, ref_state)
+        e2 += ((to_f64(o) - ref) ** 2).sum(axis=2)
+        r2 += (ref ** 2).sum(axis=2)
     torch.cuda.synchronize()
-    e_o = rel_l2(np.stack(outs), np.stack(refs))
-    e_s = rel_l2(to_f64(state.index_select(0, sel_t)), ref_state)
+    e_o = float(np.sqrt(e2.sum() / r2.sum()))
+    s64 = to_f64(state)
+    e_s = rel_l2(s64, ref_state)
+    worst_o = float(np.sqrt((e2 / r2).max()))
+    worst_s = float(np.sqrt((((s64 - ref_state) ** 2).sum(axis=(2, 3)) /
+                             (ref_state ** 2).sum(axis=(2, 3))).max()))
     tol = TOL[dtype]
+    print(f"decode rel-L2 o {e_o:.3e} state {e_s:.3e}; worst per (seq, head) o {worst_o:.3e} "
+          f"state {worst_s:.3e}")
     assert e_o <= tol, f"decode o rel-L2 {e_o:.3e} > {tol}"
     assert e_s <= tol, f"decode state rel-L2 {e_s:.3e} > {tol}"
+    assert worst_o <= 3 * tol and worst_s <= 3 * tol, (worst_o, worst_s)
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
@@ -39,11 +49,11 @@ def test_decode_small(dtype, dk, dv):
     _decode_and_score(5, 3, dk, dv, dtype, steps=6, seed=dk + dv)
 
 
-def test_decode_256_workload_sampled():
-    """256 sequences, H=32, 128 steps in place; 16 sequences scored over every step."""
-    g = torch.Generator().manual_seed(30)
-    seqs = sorted(torch.randperm(256, generator=g)[:16].tolist())
-    _decode_and_score(256, 32, 128, 128, "bf16", steps=128, seqs=seqs, seed=3)
+@pytest.mark.timeout(1800)
+def test_decode_256_workload():
+    """256 sequences, H=32, 128 steps in place: every sequence and head scored over every
+    step, and the whole state after step 128."""
+    _decode_and_score(256, 32, 128, 128, "bf16", steps=128, seed=3)
 
 
 def test_tiny_workload_as_decode_steps():
@@ -83,20 +93,31 @@ def test_prefill_then_decode_handoff(dtype):
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_decode_indexed_state_pool(dtype):
-    """Sequence n advances slot idx[n] of a state pool; other slots are untouched."""
+    """Sequence n advances slot idx[n] of a state pool: outputs and the advanced slots match
+    the fp64 oracle run on those slots' states, the result is bit-identical to dense decode
+    on the gathered states, and the other slots are untouched."""
     N, H, dk, dv, P = 4, 3, 128, 64, 7
     ds = inputs.DecodeStream(N, H, dk, dv, dtype, seed=12, device=DEV)
     g = torch.Generator(device=DEV).manual_seed(13)
     pool = torch.randn(P, H, dk, dv, device=DEV, generator=g) * 0.1
     idx = torch.tensor([5, 0, 3, 6], dtype=torch.int32, device=DEV)
     dense = pool.index_select(0, idx.long()).clone()
+    ref_state = dense.cpu().numpy().astype(np.float64)
+    A = ds.A_log.cpu().numpy().astype(np.float64)
     before = pool.clone()
+    outs, refs = [], []
     for _ in range(3):
         x = ds.step()
         o_pool = kda.decode_step_indexed(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log,
                                          pool, idx, check=True)
         o_dense = kda.decode_step(x["q"], x["k"], x["v"], x["z"], x["beta"], ds.A_log, dense)
         assert torch.equal(o_pool, o_dense)
+        h = {k: inputs.host_array(x[k]) for k in x}
+        refs.append(orc.decode(h["q"], h["k"], h["v"], h["z"], h["beta"], A, ref_state))
+        outs.append(to_f64(o_pool))
+    tol = TOL[dtype]
+    assert rel_l2(np.stack(outs), np.stack(refs)) <= tol
+    assert rel_l2(to_f64(pool.index_select(0, idx.long())), ref_state) <= tol
     assert torch.equal(pool.index_select(0, idx.long()), dense)
     untouched = [s for s in range(P) if s not in idx.tolist()]
     assert torch.equal(pool[untouched], before[untouched])
@@ -116,13 +137,18 @@ def test_decode_indexed_rejects_bad_slot():
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 def test_multi_token_decode_through_chunk_fwd(dtype):
     """k tokens per sequence against the resident state in one in-place chunked call
-    (initial_state aliasing final_state) equal k single-token decode steps."""
+    (initial_state aliasing final_state): outputs and advanced states match the fp64
+    oracle on the same packed k-token sequences, and equal k single-token decode steps."""
     N, H, dk, dv, kt = 6, 2, 128, 128, 5
     d = inputs.make_prefill([kt] * N, H=H, dk=dk, dv=dv, dtype=dtype, seed=15, h0_sigma=0.1,
                             device=DEV)
     S_multi = d["h0"].clone()
     o_multi, _ = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
                                d["cu_seqlens"], S_multi, final_state=S_multi, check=True)
+    tol = TOL[dtype]
+    ref, _, _ = oracle_prefill(d)
+    assert rel_l2(to_f64(o_multi), ref["o"]) <= tol
+    assert rel_l2(to_f64(S_multi), ref["state"]) <= tol
     S_step = d["h0"].clone()
     outs = []
     for t in range(kt):
@@ -131,6 +157,5 @@ def test_multi_token_decode_through_chunk_fwd(dtype):
         outs.append(kda.decode_step(sel["q"], sel["k"], sel["v"], sel["z"], sel["beta"],
                                     d["A_log"], S_step))
     o_step = torch.stack(outs, 1).reshape(N * kt, H, dv)
-    tol = TOL[dtype]
     assert rel_l2(to_f64(o_multi), to_f64(o_step)) <= tol
     assert rel_l2(to_f64(S_multi), to_f64(S_step)) <= tol

@@ -73,6 +73,25 @@ def test_two_calls_in_a_row_match_the_workspace_entry():
     _check_against_workspace_entry(d2, "bf16")
 
 
+def test_running_state_in_the_scratch_across_windows():
+    """Tensor-core path with final_state NULL: the running state lives in the library's
+    array beside the chunk records, and the sequence is long enough that its chunks run
+    in several windows of records, so the state crosses windows inside the array.  o
+    matches kda_chunk_fwd's."""
+    d = inputs.make_prefill([20000, 333], H=4, dk=128, dv=128, dtype="bf16", seed=44,
+                            h0_sigma=0.1, z_shift=-4.0, device=DEV)
+    T, H, dv = d["v"].shape
+    o = torch.full((T, H, dv), float("nan"), dtype=torch.bfloat16, device=DEV)
+    status = torch.full((16,), 0xFF, dtype=torch.uint8, device=DEV)
+    rc = _call_noalloc(d, o, None, status)
+    assert rc == kda.KDA_OK, kda.status_string(rc)
+    code, info = kda.query_status(status)
+    assert code == kda.KDA_OK, (kda.status_string(code), info)
+    o_ref, _ = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                             d["cu_seqlens"], d["h0"], output_final_state=False, check=True)
+    assert rel_l2(to_f64(o), to_f64(o_ref)) <= TOL["bf16"]
+
+
 def test_cuda_core_path_in_place():
     d = inputs.make_prefill([90, 33], H=2, dk=64, dv=32, dtype="f32", seed=43, h0_sigma=0.1,
                             device=DEV)

@@ -43,6 +43,7 @@ SIGNATURES = {
                                       SZ, P]),
     "kda_gate_cumsum": (I32, [P, P, P, I32, I64, I32, I32, I32, I32, I32, P, P, SZ, P]),
     "kda_query_status": (I32, [P, P, ctypes.POINTER(ctypes.c_int64)]),
+    "kda_test_chain_fault": (I32, [I64, I32]),
 }
 
 _lock = threading.Lock()

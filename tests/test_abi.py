@@ -128,3 +128,10 @@ def test_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError, match="CUDA"):
         kda.decode_step(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
                         torch.zeros(16, 1, 32, 32))
+
+
+def test_fault_hook_rejects_a_non_positive_limit(lib):
+    """The bounded-wait test hook validates its limit on the host (nothing is armed)."""
+    from gated_delta_rule_43_gb300 import kda
+    assert lib.kda_test_chain_fault(0, 0) == kda.KDA_ERR_INVALID_ARG
+    assert lib.kda_test_chain_fault(-5, -1) == kda.KDA_ERR_INVALID_ARG

@@ -1,7 +1,9 @@
 """The standalone gate kernel and device-side error reporting (GPU).
 
 Errors are provoked with bad INPUT values (NaN in z, inconsistent
-cu_seqlens) that the kernels check themselves; nothing here faults a GPU.
+cu_seqlens) that the kernels check themselves, or with the library's test hook
+that leaves out one record load so that a bounded device wait (1 ms) expires;
+nothing here faults or hangs a GPU.
 """
 import numpy as np
 import pytest
@@ -109,3 +111,27 @@ def test_tensor_core_path_bad_cu_seqlens_are_reported():
     o, s = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
                          d["cu_seqlens"], check=True)
     assert torch.isfinite(o).all() and torch.isfinite(s).all()
+
+
+def test_expired_chain_wait_is_reported_and_the_next_call_is_clean():
+    """The test hook leaves out the first record load of chain CTA 0 and gives every wait of
+    the chain a 1 ms limit: that CTA's wait expires before it has issued any product, it
+    reports KDA_ERR_TIMEOUT (info = its item, sequence 0 / head 0 / column block 0), lets the
+    load it did issue finish and leaves.  The next call on the same workspace, without the
+    hook, matches the oracle."""
+    from tests.gpu_util import TOL, score_prefill
+    d = inputs.make_prefill([500, 300], H=2, dk=128, dv=128, dtype="bf16", seed=50,
+                            h0_sigma=0.1, device=DEV)
+    T, H, dk = d["q"].shape
+    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, 2, H, dk, 128, torch.bfloat16),
+                             DEV)
+    lib = kda.load()
+    assert lib.kda_test_chain_fault(1_000_000, 0) == kda.KDA_OK
+    kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"], d["cu_seqlens"],
+                  d["h0"], workspace=ws)
+    code, info = kda.query_status(ws)
+    assert code == kda.KDA_ERR_TIMEOUT and info == 0, (kda.status_string(code), info)
+    o, hT = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
+                          d["cu_seqlens"], d["h0"], workspace=ws, check=True)
+    e_o, e_s = score_prefill(d, o, hT)
+    assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (e_o, e_s)

@@ -130,12 +130,11 @@ ChunkLayout chunk_layout_seg(int64_t T, int32_t N, int32_t H, int32_t dk, int32_
 }
 
 // The segment count kda_chunk_fwd picks by itself on the tensor-core path: the largest
-// s <= 16 whose first pass, N H (2 + 4 (s - 1)) chain CTAs (64 value columns each), still
-// fits in half of the current device's SMs while the average sequence keeps >= 64 chunks
-// per segment; 1 (the plain schedule) when even s = 2 does not qualify.  The benchmark
-// workloads (8K with 32 heads, 1M with 16, 64 packed sequences) stay plain: their windows
-// run with the prep of the next window beside the chain, which the segmented schedule
-// (windows one after the other) gives up.
+// s <= 16 whose first pass, N H (4 + 8 (s - 1)) 32-column CTAs, still fits one wave of
+// the current device's SMs while the average sequence keeps >= 64 chunks per segment;
+// 1 (the plain schedule) when even s = 2 does not qualify.  Measured: one 1M-token
+// sequence with 4 heads runs in 10.1 ms with 5 segments against 16.0 ms plain; the
+// benchmark workloads (8K with 32 heads, 1M with 16, 64 packed sequences) stay plain.
 int32_t auto_segments(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv, int32_t dtype) {
     if (!use_tc(dtype, dk, dv) || N <= 0 || T <= 0) return 1;
     int dev = 0, sms = 0;
@@ -146,7 +145,7 @@ int32_t auto_segments(int64_t T, int32_t N, int32_t H, int32_t dk, int32_t dv, i
     const int64_t chunks = T / ((int64_t)kTcChunk * N);   // whole chunks of the average sequence
     int32_t best = 1;
     for (int32_t s = 2; s <= 16; ++s) {
-        if (2 * pairs * (2 + 4 * (s - 1)) > sms || chunks < 64 * (int64_t)s) break;
+        if (pairs * (4 + 8 * (s - 1)) > sms || chunks < 64 * (int64_t)s) break;
         best = s;
     }
     return best;

@@ -10,14 +10,10 @@
 //   W  = T diag(b) (K*Gam),  Ut = T diag(b) V,  U = Ut - W S
 //   O  = (Q*Gam) S + P U,    P = lower_incl( [(q_r*Gam_r).(k_j/Gam_j)] )
 //   S <- Diag(Gam_C) S + (K*Gam_C/Gam)^T U
-// Everything S-independent runs in a parallel "prep" kernel over all (chunk, head) pairs,
-// which also folds the chunk into an affine map of the state and an affine map of the
-// outputs (U = Ut - W S substituted):
-//   S <- Diag(Gam_C) S + Mn S + B,    Mn = -(K*Gam_C/Gam)^T W,  B = (K*Gam_C/Gam)^T Ut
-//   O  = Q' S + Y,                    Q' = Q*Gam - P W,         Y = P Ut
-// so that a "chain" kernel, walking the chunks in order, has a single dependent product
-// (Mn S) per chunk; Q' S runs beside it and is consumed a chunk later.  The chain runs
-// one CTA per (sequence, head, 64-column block of dv).
+// Everything but the last three products is independent of S, so it runs in
+// a parallel "prep" kernel over all (chunk, head) pairs; a "chain" kernel then walks
+// the chunks in order, one CTA per (sequence, head, 32-column block of dv) or, when
+// there are many sequences, per (sequence, head) with all 128 columns.
 //
 // Numerics (the page's point about 16-token tiles): exp(G_r - G_j) is never
 // formed from a chunk-global exp(-G).  For row r in 16-token tile a, with
@@ -29,13 +25,13 @@
 // the same row-scaled [K;Q] tile block by its own column-scaled K block.
 // W, Q*Gam and K*Gam_C/Gam use exp(G) <= 1 directly.
 //
-// Prep output per (chunk slot, head): one record that the chain kernel reads:
-//   MQ  K-major [192 rows][128 K] bf16, 128-byte swizzle (a shared-memory operand image,
-//       copied with one 1-D bulk copy): rows 0-127 Mn, rows 128-191 Q'
-//   GC  fp32 [128] Gam_C (copied with MQ)
-//   B   bf16 [2 column blocks][128 rows][64], row-major within a block
-//   Y   bf16 [2 column blocks][64 rows][64], row-major within a block
-// (B and Y are read by each chain thread straight into registers, a chunk ahead.)
+// Prep output per (chunk slot, head): one record of smem images (128-byte
+// swizzle) that the chain kernel copies with 1-D bulk TMA:
+//   WQ  K-major [128 rows][128 K]: rows 0-63 W, rows 64-127 Q*Gam
+//   KT  MN-major [64 k-rows][128 m]: K*Gam_C/Gam, read as the M=dk x K=C operand
+//   P   K-major [64][64]
+//   Ut  fp32 [4 column blocks][64][32], float4 slot j4 of row r holds columns 4 (j4 ^ (r % 8))
+//   GC  fp32 [128] Gam_C
 #include <cuda.h>
 #include <string.h>
 
@@ -54,14 +50,12 @@ constexpr int C = 64;            // chunk length (four 16-token tiles)
 constexpr int DK = 128, DV = 128;
 
 // record layout (bytes)
-constexpr uint32_t REC_MQ = 0;
-constexpr uint32_t MQ_ROWS = 192;
-constexpr uint32_t REC_G = 49152;
-constexpr uint32_t REC_B = 49664;
-constexpr uint32_t REC_Y = REC_B + 2 * 16384;
-constexpr uint32_t REC_BYTES = REC_Y + 2 * 8192;   // 98816
-static_assert(REC_G == MQ_ROWS * 128 * 2 && REC_B == REC_G + 512 && REC_BYTES % 256 == 0,
-              "record layout");
+constexpr uint32_t REC_WQ = 0;
+constexpr uint32_t REC_KT = 32768;
+constexpr uint32_t REC_P = 49152;
+constexpr uint32_t REC_U = 57344;
+constexpr uint32_t REC_G = 90112;
+constexpr uint32_t REC_BYTES = 90624;
 
 // ---------------------------------------------------------------- prep kernel
 constexpr int PREP_THREADS = 256;
@@ -90,25 +84,24 @@ constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
 constexpr uint32_t P_ZT = 47104;        // (until pass A) z tile, TMA, [2][64][128 B] swizzled
 constexpr uint32_t P_KT = 63488;        // (until the table pass) k tile, likewise
 constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewise
-constexpr uint32_t P_PI = 1024;         // (A/P epilogue .. step E) P, K-major [64][64], over the dead tables
-constexpr uint32_t P_KTI = 87040;       // (pass B .. step E) K*Gam_C/Gam, MN-major [64 k][128 m]
-constexpr uint32_t P_TB = 104448;       // (solve .. step E) K-major [64][64] T diag(b)
-constexpr uint32_t P_RI = 46080;        // (step E .. G) K-major [192][64]: rows 0-63 R2, 64-191 R
-constexpr uint32_t P_END = 112640;
+constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], over the dead tables
+constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
+constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
+constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, fp32 [4][64][32]
+constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
+constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
 constexpr uint32_t P_SMEM = P_END + 1024;
-static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_KTI, "column-scaled K images overflow");
+static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
-static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_KTI, "solve scratch");
-static_assert(P_G + 64 * GLD * 4 <= P_ZT, "G scratch overlaps the raw tiles");
-static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_TB && P_ZT % 1024 == 0 &&
+static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
+static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
+static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
                   P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
-static_assert(P_PI + 8192 + 8192 <= P_KGV + 32768 && P_PI + 8192 <= P_BETA,
-              "P image (and the 64 rows an M = 128 operand reads after it)");
-static_assert(P_KTI + 16384 <= P_TB && P_TB + 8192 <= P_END && P_RI + 24576 <= P_KTI,
-              "K~, T diag(b) and R images");
-static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0 && P_KTI % 1024 == 0 &&
-                  P_RI % 1024 == 0 && P_PI % 1024 == 0, "image alignment");
-static_assert(2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
+static_assert(P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
+                  P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
+              "solve / epilogue staging overlaps live data");
+static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
+static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
     *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
@@ -302,9 +295,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     }
     __syncthreads();
 
-    // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr], column-scaled K images and
-    //          K*Gam_C/Gam (smem), Q*Gam (straight into the Q' rows of the record's MQ image,
-    //          where the output-map epilogue reads it back)
+    // ---- (B) decay-scaled operands, 16-byte stores: [Kr; Qr] (smem), column-scaled K
+    //          images (smem), Q*Gam and K*Gam_C/Gam (straight into the record)
     uint4 kgam[NU];   // K*Gam chunks, written into the [K*Gam | V] image after the A/P products
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
@@ -331,8 +323,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const uint32_t row = 32 * a + rl;
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row, c, 128)) = pack8(kr);
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
-        *reinterpret_cast<uint4 *>(rec + REC_MQ + sw128_offset(128 + r, c, MQ_ROWS)) = pack8(qg);
-        *reinterpret_cast<uint4 *>(sm + P_KTI + sw128_offset(r, c, 64)) = pack8(kt);
+        *reinterpret_cast<uint4 *>(sm + P_QST + sw128_offset(r, c, 64)) = pack8(qg);
+        *reinterpret_cast<uint4 *>(rec + REC_KT + sw128_offset(r, c, 64)) = pack8(kt);
         // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a);
         // image a2 occupies rows 8 a2 (a2 + 1) .. of the stacked [160][128] B operand
         *reinterpret_cast<uint4 *>(sm + P_KC + sw128_offset(8 * a * (a + 1) + r, c, KC_ROWS)) = pack8(kf);
@@ -365,6 +357,12 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             umma_commit(&bar[0]);
         }
         __syncwarp();
+        if (lane == 0) {
+            // Q*Gam (staged in pass B) -> rows 64..127 of the record's WQ image, both K halves
+            bulk_s2g(rec + REC_WQ + 8192, sm + P_QST, 8192);
+            bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
+            bulk_commit();
+        }
     }
     ok = mbar_wait(&bar[0], 0) && ok;
     tc_fence_after();
@@ -379,7 +377,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
     for (int u = 0; u < NU; ++u)
         *reinterpret_cast<uint4 *>(sm + P_KGV + sw128_offset(16 * u + rl, c, 64)) = kgam[u];
-    // A (fp32, smem) and P (bf16 image, smem: the A operand of step E) from TMEM:
+    // A (fp32, smem) and P (bf16 image, straight into the record) from TMEM:
     // warp w reads its own lane quarter t = w & 3 (rows 32t.. of D_t: 16 Kr rows, then
     // 16 Qr rows), column blocks m = 2 (w >> 2) and 2 (w >> 2) + 1 of D_t
     float *AS = reinterpret_cast<float *>(sm + P_AS);
@@ -422,7 +420,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                         const int j = 16 * m + 8 * half + i;
                         x[i] = (j <= rr) ? val[mm][8 * half + i] : 0.f;
                     }
-                    *reinterpret_cast<uint4 *>(sm + P_PI + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
+                    *reinterpret_cast<uint4 *>(sm + P_PST + sw128_offset(rr, 16 * m + 8 * half, 64)) = pack8(x);
                 }
             }
         }
@@ -430,13 +428,18 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
+    if (tid == 0) {                       // P -> the record
+        bulk_s2g(rec + REC_P, sm + P_PST, 8192);
+        bulk_commit();
+    }
 
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
     //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
-    // The T diag(b) image (K-major [64][64] bf16, the B operand of step E) is written in two
-    // steps: zero blocks above the diagonal in the N^3 step, the other blocks in the last
-    // step of the solve.
+    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E) shares its region
+    // with the Q*Gam staging, whose bulk copy is given until the N^3 step to finish; it is
+    // written there: zero blocks above the diagonal in the N^3 step, the other blocks in
+    // the last step of the solve.
     uint8_t *TBI = sm + P_TB;
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
     auto pair_a = [](int pr) { return pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3); };
@@ -492,6 +495,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
     }
+    if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
     __syncthreads();
     if (tid < 64) {  // N^3_30 = N32 N^2_20
         const int i = tid >> 2, jq = tid & 3;
@@ -559,163 +563,66 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     tc_fence_before();
     __syncthreads();
 
-    // ---- (E) R = (K*Gam_C/Gam)^T T diag(b) (M = dk = 128, N = 64) into TMEM columns 0..63,
-    //          R2 = P T diag(b) into columns 64..127 (rows 0..63 of an M = 128 product whose
-    //          A operand reads 64 unused rows after P).  T diag(b) is the B operand: its
-    //          K-major image read as MN-major (k = row of T).
+    // ---- (E) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
     if (warp == 0) {
+        ok = mbar_wait(vbar, 0) && ok;
         tc_fence_after();
-        const uint32_t id_r = idesc_bf16(128, 64, true, true);     // A MN-major (K~ image)
-        const uint32_t id_r2 = idesc_bf16(128, 64, false, true);   // A K-major (P image)
-        const uint64_t akt = sdesc_sw128(base + P_KTI, 64 * 128, 1024);
-        const uint64_t ap = sdesc_sw128(base + P_PI, 16, 1024);
-        const uint64_t btb = sdesc_sw128(base + P_TB, 64 * 128, 1024);
+        const uint32_t idesc = idesc_bf16(128, 256, false, true);
+        const uint64_t ad = sdesc_sw128(base + P_TB, 16, 1024);
+        const uint64_t bd = sdesc_sw128(base + P_KGV, 64 * 128, 1024);
         if (elect_one()) {
 #pragma unroll
             for (int s = 0; s < C / 16; ++s)
-                umma_bf16(tmem, desc_add(akt, s * 2048), desc_add(btb, s * 2048), id_r, s > 0);
-#pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                umma_bf16(tmem + 64, desc_add(ap, s * 32), desc_add(btb, s * 2048), id_r2, s > 0);
+                umma_bf16(tmem, desc_add(ad, s * 32), desc_add(bd, s * 2048), idesc, s > 0);
             umma_commit(&bar[1]);
         }
         __syncwarp();
     }
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
-    // R and R2 -> one K-major [192][64] bf16 image: rows 0-63 R2, rows 64-191 R.  Warp w
-    // reads lane quarter t = w & 3, columns 32 (w >> 2) ..
-    {
-        const int t = warp & 3, hh = warp >> 2;
-        const int rr = 32 * t + lane;
-        const uint32_t src = tmem + ((uint32_t)(32 * t) << 16) + 32 * hh;
-        float x[32], y[32];
-        tmem_ld32(src, x);
-        if (t < 2) tmem_ld32(src + 64, y);
-        tmem_ld_wait();
+
+    // ---- (F) W rows (K-major, rows 0..63 of the record's WQ image) and Ut (fp32) are staged
+    //          in the freed shared memory and leave in three bulk copies.  Rows 0..63 live in
+    //          lane quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut)
+    //          x (32-column block), two 16-column TMEM loads in flight per wait.
+    uint8_t *WST = sm + P_WST;   // [2 K halves][64 rows][128 B]
+    uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] fp32, slots swizzled
+    if ((warp & 3) < 2) {
+        const int quarter = warp & 3;
+        const int rr = 32 * quarter + lane;
+        const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16);
+        for (int task = warp >> 2; task < 8; task += PREP_WARPS / 4) {
+            const bool isW = task < 4;
+            const int cb = task & 3;
+            float lo[16], hi[16];
+            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb, lo);
+            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb + 16, hi);
+            tmem_ld_wait();
+            if (isW) {
 #pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            float v[8];
+                for (int i8 = 0; i8 < 4; ++i8) {
+                    float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] = x[8 * c8 + e];
-            *reinterpret_cast<uint4 *>(sm + P_RI + sw128_offset(64 + rr, 32 * hh + 8 * c8, 192)) = pack8(v);
-        }
-        if (t < 2) {
+                    for (int i = 0; i < 8; ++i) x[i] = i8 < 2 ? lo[8 * i8 + i] : hi[8 * (i8 - 2) + i];
+                    *reinterpret_cast<uint4 *>(WST + sw128_offset(rr, 32 * cb + 8 * i8, 64)) = pack8(x);
+                }
+            } else {
+                // row rr of column block cb; float4 j4 stored at slot j4 ^ (rr % 8) so that the
+                // chain kernel's row-per-thread reads hit distinct banks
+                float4 *dst = reinterpret_cast<float4 *>(UST + ((cb * 64 + rr) * 32) * 4);
 #pragma unroll
-            for (int c8 = 0; c8 < 4; ++c8) {
-                float v[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = y[8 * c8 + e];
-                *reinterpret_cast<uint4 *>(sm + P_RI + sw128_offset(rr, 32 * hh + 8 * c8, 192)) = pack8(v);
+                for (int i4 = 0; i4 < 8; ++i4) {
+                    const float *v4 = i4 < 4 ? lo + 4 * i4 : hi + 4 * (i4 - 4);
+                    dst[i4 ^ (rr & 7)] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+                }
             }
         }
     }
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();
-
-    // ---- (G1) [-Mn | B] = R [K*Gam | V]  (M = 128, N = 256, K = 64): the state map
-    const uint32_t id_g = idesc_bf16(128, 256, false, true);
-    const uint64_t bd_kgv = sdesc_sw128(base + P_KGV, 64 * 128, 1024);
-    if (warp == 0) {
-        ok = mbar_wait(vbar, 0) && ok;
-        tc_fence_after();
-        const uint64_t ar = sdesc_sw128(base + P_RI + 64 * 128, 16, 1024);
-        if (elect_one()) {
-#pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                umma_bf16(tmem, desc_add(ar, s * 32), desc_add(bd_kgv, s * 2048), id_g, s > 0);
-            umma_commit(&bar[0]);
-        }
-        __syncwarp();
-    }
-    ok = mbar_wait(&bar[0], 1) && ok;
-    tc_fence_after();
-    // warp w: rows 32 (w & 3) .. of the map (state row i), columns 0..127 (Mn, negated, into
-    // the record's MQ image) or 128..255 (B, row-major per 64-column block)
-    {
-        const int t = warp & 3, hh = warp >> 2;
-        const int i = 32 * t + lane;
-        const uint32_t src = tmem + ((uint32_t)(32 * t) << 16) + 128 * hh;
-#pragma unroll
-        for (int cq = 0; cq < 4; cq += 2) {
-            float x[2][32];
-            tmem_ld32(src + 32 * cq, x[0]);
-            tmem_ld32(src + 32 * cq + 32, x[1]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int col = 32 * (cq + u);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float v[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) v[e] = hh == 0 ? -x[u][8 * c8 + e] : x[u][8 * c8 + e];
-                    uint8_t *dst = hh == 0
-                        ? rec + REC_MQ + sw128_offset(i, col + 8 * c8, MQ_ROWS)
-                        : rec + REC_B + (col >> 6) * 16384 + i * 128 + ((col & 63) + 8 * c8) * 2;
-                    *reinterpret_cast<uint4 *>(dst) = pack8(v);
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-
-    // ---- (G2) [P W | P Ut] = R2 [K*Gam | V]: rows 0..63 of an M = 128 product whose A
-    //           operand is the [R2; R] image from row 0 (rows 64.. of the result are unused)
-    if (warp == 0) {
-        tc_fence_after();
-        const uint64_t ar2 = sdesc_sw128(base + P_RI, 16, 1024);
-        if (elect_one()) {
-#pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                umma_bf16(tmem, desc_add(ar2, s * 32), desc_add(bd_kgv, s * 2048), id_g, s > 0);
-            umma_commit(&bar[1]);
-        }
-        __syncwarp();
-    }
-    ok = mbar_wait(&bar[1], 1) && ok;
-    tc_fence_after();
-    // the output map: Q' = Q*Gam - P W over the Q*Gam rows pass B left in the record, and
-    // Y = P Ut (row-major per 64-column block); lane quarters 0-1 hold the 64 token rows
-    if ((warp & 3) < 2) {
-        const int t = warp & 3, hh = warp >> 2;
-        const int r = 32 * t + lane;
-        const uint32_t src = tmem + ((uint32_t)(32 * t) << 16) + 128 * hh;
-#pragma unroll
-        for (int cq = 0; cq < 4; cq += 2) {
-            float x[2][32];
-            tmem_ld32(src + 32 * cq, x[0]);
-            tmem_ld32(src + 32 * cq + 32, x[1]);
-            tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const int col = 32 * (cq + u);
-#pragma unroll
-                for (int c8 = 0; c8 < 4; ++c8) {
-                    float v[8];
-                    uint8_t *dst;
-                    if (hh == 0) {
-                        dst = rec + REC_MQ + sw128_offset(128 + r, col + 8 * c8, MQ_ROWS);
-                        float qv[8];
-                        unpack8(*reinterpret_cast<const uint4 *>(dst), qv);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = qv[e] - x[u][8 * c8 + e];
-                    } else {
-                        dst = rec + REC_Y + (col >> 6) * 8192 + r * 128 + ((col & 63) + 8 * c8) * 2;
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) v[e] = x[u][8 * c8 + e];
-                    }
-                    *reinterpret_cast<uint4 *>(dst) = pack8(v);
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    // An expired wait: let every product this CTA issued and every tile load finish (each
-    // wait bounded again) before the tensor memory is released and the CTA leaves.
     if (!__syncthreads_and(ok)) {
+        // an expired wait: every product this CTA issued and every tile load finishes
+        // (each wait bounded again) before the tensor memory is released
         if (warp == 0) {
             tc_fence_after();
             if (elect_one()) umma_commit(drain);
@@ -733,6 +640,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
+        if (lane == 0) {
+            bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
+            bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
+            bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
+            bulk_commit();
+            // the CTA may leave once the staging has been read; the writes complete with
+            // the kernel, before anything ordered after it reads the records
+            bulk_wait_read_all();
+        }
     }
 }
 
@@ -771,58 +687,68 @@ __device__ __forceinline__ void seg_range(int32_t c0, int32_t L, int segs, int k
     e = c0 + (int32_t)(((int64_t)(k + 1) * L) / s_eff);
 }
 
-// ------------------------------------------------ chain kernel (affine form)
-// One CTA per (sequence, head, 64-column block of dv): two per head.  Per chunk the only
-// dependent product is D_S = Mn S (M = 128, N = 64, K = 128); the output product
-// D_O = [Mn rows 64..127; Q'] S is issued behind it and read a chunk later.
-namespace ac {
-
-constexpr int DVB = 64;                          // value columns per CTA
-constexpr int NBLK = DV / DVB;                   // CTAs per (sequence, head)
-constexpr int THREADS = 256;                     // warp w: lane quarter w % 4, columns 32 (w / 4) ..
-constexpr int NBUF = 3;                          // record buffers (MQ image and Gam_C)
-constexpr uint32_t LOAD_BYTES = REC_B;           // MQ and Gam_C: one bulk copy
-constexpr uint32_t BUF_BYTES = (LOAD_BYTES + 1023) / 1024 * 1024;
-constexpr uint32_t S_BYTES = DK * DVB * 2;       // S image, MN-major SW128 [128 k][64 n]
-constexpr uint32_t C_S = NBUF * BUF_BYTES;       // two S images
-constexpr uint32_t C_BAR = C_S + 2 * S_BYTES;    // full[3], dS, dO[2], drain; TMEM slot, flags
-constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
-constexpr uint32_t TMEM_COLS = 256;              // D_S at column 0, D_O at 64 and 128
-constexpr uint32_t B_BLK = 16384, Y_BLK = 8192;  // bytes of one 64-column block of B and Y
-static_assert(BUF_BYTES % 1024 == 0 && C_S % 1024 == 0 && C_SMEM <= 232448, "chain smem");
-static_assert(LOAD_BYTES % 16 == 0, "bulk copy size");
-
 // Test hook: a bounded wait limit and a record load to leave out (so that the wait for it
-// expires), given per launch.
+// expires), given per launch of a chain kernel.
 struct Fault {
-    uint64_t wait_ns;    // limit of every bounded wait
+    uint64_t wait_ns;    // limit of every bounded wait of the chain kernel
     int skip_cta;        // CTA whose first record load is not issued (-1: none)
 };
 
-__device__ __forceinline__ void load_rec(uint8_t *buf, const uint8_t *rec, uint64_t *full) {
+// ------------------------------------------------ chain kernel, 32-column blocks
+// The latency-bound shape: one CTA per (sequence, head, 32-column block of dv).  The
+// N = 32 products finish sooner than N = 128 ones, so a lone long sequence walks its
+// chunks fastest with four narrow CTAs per head.
+namespace c32 {
+
+constexpr int DVB = 32;          // value columns per CTA
+constexpr int DK_ROWS = DK;      // threads of the scan kernel (one per state row)
+constexpr int NBLK = DV / DVB;
+constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x; P] U
+// a record buffer mirrors the record's first 57344 bytes (WQ, KT, P), then this CTA's U
+// block and Gam_C
+constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = 65536;
+constexpr uint32_t BUF_BYTES = 66560;
+constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
+constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
+constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, m3, drain; TMEM slot, flags
+constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
+constexpr uint32_t LOAD_BYTES = REC_U + 8192 + 512;
+static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0 && B_P == REC_P && B_KT == REC_KT,
+              "chain buffer layout");
+static_assert(C_S % 1024 == 0 && C_UI % 1024 == 0, "operand image alignment");
+static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
+
+__device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int blk,
+                                           uint64_t *full) {
     mbar_arrive_expect_tx(full, LOAD_BYTES);
-    bulk_g2s(buf, rec, LOAD_BYTES, full);
+    bulk_g2s(buf, rec, REC_U, full);   // WQ, KT, P in one copy
+    bulk_g2s(buf + B_U, rec + REC_U + blk * 8192, 8192, full);
+    bulk_g2s(buf + B_G, rec + REC_G, 512, full);
 }
 
-// 32 bf16 of a row-major 64-column block row (B or Y) -> 4 x 16 bytes, through the
-// read-only path (records are written by an earlier kernel)
-__device__ __forceinline__ void ld_row32(const uint8_t *p, uint4 (&v)[4]) {
+// 32 fp32 values -> four 16-byte chunks of row r of a 64B-swizzled MN-major image
+__device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float (&x)[32]) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = __ldg(reinterpret_cast<const uint4 *>(p) + k);
+    for (int c8 = 0; c8 < 4; ++c8) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = x[8 * c8 + i];
+        *reinterpret_cast<uint4 *>(img + sw64_offset(r, 8 * c8, 1)) = pack8(y);
+    }
 }
 
-// Persistent over work items (sequence, head, 64-column block) of the sequences that own
-// chunks in the slot window [slot0, slot1); each item walks its chunks in order, carrying
-// its block of S in registers (fp32; thread (quarter q, group g) holds row 32 q + lane,
-// columns 32 g .. 32 g + 31) and as the bf16 B operand image.  Per chunk c:
-//   D_S = Mn S_c                       (critical)      S_{c+1} = Diag(Gam_C) S_c + D_S + B
-//   D_O = [Mn(64..127); Q'] S_c        (rows 64.. are O - Y, read during chunk c + 1)
-// Record buffers rotate over three slots so that the MQ image of chunk c + 2 is in flight
-// while chunk c runs; each thread reads its B row of chunk c + 1 and (rows 64..127) its Y
-// row of chunk c into registers a chunk ahead.  In the segment-parallel modes (SegArgs) an
-// item is one segment of a sequence's chunks in the window, and a map item walks a block
-// of [M | B] from [I | 0] (B added only to the B columns) without outputs.
-__global__ void __launch_bounds__(THREADS, 1)
+// Persistent over work items (sequence, head, 32-column block) of the sequences
+// that own chunks in the slot window [slot0, slot1); each item walks its chunks
+// in order, carrying its block of S in registers (fp32, thread i = row i) and as
+// the bf16 B operand image.  Per chunk, on the critical path:
+//   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
+//   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
+// D1 is double-buffered in TMEM so that the output rows of chunk c (D1[64:128])
+// are stored by warps 2-3 while warps 0-1 form U of chunk c+1.  In the segment-parallel
+// modes (SegArgs) an item is one segment of a sequence's chunks in the window, and a map
+// item walks a 32-column block of [M | B] from [I | 0] (Ut = 0 for the M columns)
+// without storing outputs.
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
 chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
              int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
              const float *h0, float *__restrict__ state, __nv_bfloat16 *__restrict__ o,
@@ -841,46 +767,37 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const int items = (n_last - n_first + 1) * H * ipp;
     if ((int)blockIdx.x >= items) return;
 
-    uint64_t *full = reinterpret_cast<uint64_t *>(sm + C_BAR);          // [NBUF]
-    uint64_t *dS = full + NBUF;                                         // D_S done
-    uint64_t *dO = dS + 1;                                              // [2] D_O done
-    uint64_t *drain = dO + 2;                                           // everything issued
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 64);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 68);
-    uint32_t *ld_issued = reinterpret_cast<uint32_t *>(sm + C_BAR + 80);   // [NBUF] loads issued
-    uint32_t *ld_done = ld_issued + NBUF;                                   // [NBUF] and waited
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3, drain
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 48);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 52);
+    // record loads issued into / seen complete in buffers 0 and 1: kept in registers by
+    // thread 64, which issues every load (shared-memory counters beside the barriers
+    // measured 0.5 us a chunk slower)
+    uint32_t iss0 = 0, iss1 = 0, don0 = 0, don1 = 0;
+    const uint64_t lim = flt.wait_ns;
     if (tid == 0) {
-        for (int x = 0; x < NBUF + 4; ++x) mbar_init(&full[x], 1);
+        for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
+        mbar_init(&bar[5], 2);   // one commit from each issuing warp (0 and 4)
         *abort_flag = 0;
-        for (int x = 0; x < NBUF; ++x) ld_issued[x] = ld_done[x] = 0;
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(tslot, TMEM_COLS);
+        tmem_alloc(tslot, 128);
         tmem_relinquish();
         tc_fence_before();
     }
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    const int q4 = warp & 3, cg = warp >> 2;
-    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const uint32_t D2 = tmem + 64;                     // D1 buffers at columns 0 and 32
+    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
     const uint32_t base = smem_u32(sm);
-    const uint32_t idesc = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
-    const int i = 32 * q4 + lane;      // this thread's state row
-    const int cl = 32 * cg;            // and first column within the block
-    const bool out_thread = q4 >= 2;   // D_O rows 64..127 are the chunk's 64 outputs
-    const uint64_t lim = flt.wait_ns;
-    uint32_t gi = 0;                   // chunks walked by this CTA: buffer gi % 3, parities
-    uint32_t go = 0;                   // output products issued by this CTA: D_O buffer go & 1
-    bool first_item = true;
-
-    // issue the load of record `c` into buffer `slot` (one thread)
-    auto issue_load = [&](int32_t c, int h, uint32_t slot) {
-        load_rec(sm + slot * BUF_BYTES, records + ((size_t)(c - slot0) * H + h) * REC_BYTES,
-                 &full[slot]);
-        ld_issued[slot] += 1;
-    };
+    const uint32_t id_km = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
+    const uint32_t id_mm = idesc_bf16(128, DVB, true, true);    // A MN-major, B MN-major
+    const uint64_t bd_s = sdesc_sw64(base + C_S, 128 * 64, 512);    // S image, K step 0
+    const uint64_t bd_u = sdesc_sw64(base + C_UI, 64 * 64, 512);    // U image, K step 0
+    const int i = tid;  // this thread's state row
+    uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
     for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
         const int r_it = item % ipp;
@@ -913,192 +830,198 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         }
         const int64_t bos = cu[n];
         const int64_t eos = cu[n + 1];
-        const int j0 = blk * DVB + cl;     // this thread's first column of S (or of M / B)
+        const int j0 = blk * DVB;
+        float S[DVB];
         const int64_t pairoff = (int64_t)n * H + h;
         const int64_t soff = (pairoff * DK + i) * DV + j0;
         float *srow = state + soff;
-        auto rec_of = [&](int32_t c) { return records + ((size_t)(c - slot0) * H + h) * REC_BYTES; };
-        // B row of chunk c (zero for the M columns of a map) and Y row of chunk c
-        auto load_b = [&](int32_t c, uint4 (&v)[4]) {
-            if (mpart) {
+        // the sequence's first chunk starts from h0 (zeros when absent), later windows from
+        // the running state, a later segment from its composed start state, a map from
+        // the identity (M columns) or zeros (B columns)
+        const float *s_in = map ? nullptr
+                          : seg > 0 ? sa.start + ((pairoff * sa.segs + seg) * DK + i) * DV + j0
+                          : w_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
+        if (warp < 4) {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) v[k] = make_uint4(0, 0, 0, 0);
-            } else {
-                ld_row32(rec_of(c) + REC_B + blk * B_BLK + i * 128 + cl * 2, v);
-            }
-        };
-        auto load_y = [&](int32_t c, uint4 (&v)[4]) {
-            ld_row32(rec_of(c) + REC_Y + blk * Y_BLK + (i - 64) * 128 + cl * 2, v);
-        };
-        float S[32];
-        {
-            // the sequence's first chunk starts from h0 (zeros when absent), later windows
-            // from the running state, a later segment from its composed start state, a map
-            // from the identity (M columns) or zeros (B columns)
-            const float *s_in = map ? nullptr
-                              : seg > 0 ? sa.start + ((pairoff * sa.segs + seg) * DK + i) * DV + j0
-                              : w_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
-#pragma unroll
-            for (int j4 = 0; j4 < 8; ++j4) {
+            for (int j4 = 0; j4 < DVB / 4; ++j4) {
                 const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
             }
             if (mpart) {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) S[j] = (i == j0 + j) ? 1.f : 0.f;
+                for (int j = 0; j < DVB; ++j) S[j] = (i == j0 + j) ? 1.f : 0.f;
             }
+            store_row_sw64(sm + C_S, i, S);
+            fence_proxy_async();
         }
-        // S image of the item's first chunk
-#pragma unroll
-        for (int c8 = 0; c8 < 4; ++c8) {
-            float y[8];
-#pragma unroll
-            for (int x = 0; x < 8; ++x) y[x] = S[8 * c8 + x];
-            *reinterpret_cast<uint4 *>(sm + C_S + (gi & 1) * S_BYTES + sw128_offset(i, cl + 8 * c8, DK)) =
-                pack8(y);
-        }
-        fence_proxy_async();
         __syncthreads();
-        if (tid == 0) {
-            const bool skip = first_item && (int)blockIdx.x == flt.skip_cta;
-            if (!skip) issue_load(c_begin, h, gi % NBUF);
-            if (c_begin + 1 < c_end) issue_load(c_begin + 1, h, (gi + 1) % NBUF);
+        if (tid == 64 && !(item == (int)blockIdx.x && (int)blockIdx.x == flt.skip_cta)) {
+            chain_load(sm + (gi & 1) * BUF_BYTES,
+                       records + ((size_t)(c_begin - slot0) * H + h) * REC_BYTES, blk,
+                       &bar[gi & 1]);
+            iss0 += (gi & 1) == 0;
+            iss1 += (gi & 1) == 1;
         }
-        first_item = false;
-        uint4 bcur[4], bnext[4], ycur[4];
-        load_b(c_begin, bcur);
 
-        bool ok = true;
+        // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
+        // (warps 2-3); waits for that chunk's [x; P] U product (barrier m3)
+        auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
+            const uint32_t pb = gprev & 1;
+            if (!mbar_wait(&bar[4], gprev & 1, lim)) return false;
+            tc_fence_after();
+            const int r = tid - 64;
+            const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
+            float oacc[32];
+            tmem_ld32(tmem + 32 * pb + lane_base, oacc);
+            tmem_ld_wait();
+            if (t < eos && !map) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8) {
+                    float y[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) y[x] = oacc[8 * i8 + x];
+                    dst[i8] = pack8(y);
+                }
+            }
+            return true;
+        };
+
+        bool aborted = false;
         for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
-            const uint32_t b = gi % NBUF, sb = gi & 1;
+            const uint32_t b = gi & 1;
+            uint8_t *buf = sm + b * BUF_BYTES;
             const uint32_t bufa = base + b * BUF_BYTES;
-            if (cs + 1 < c_end) load_b(cs + 1, bnext);
-            ok = mbar_wait(&full[b], (gi / NBUF) & 1, lim);
-            if (tid == 0 && ok) ld_done[b] += 1;
+            if (warp == 4) {
+                // D1[b] += [x; P] U (outputs only), issued behind D2 so that it runs while S is
+                // updated; warp 4 joins no per-chunk barrier.  [x; P] reads the 64 rows in
+                // front of P (the tail of KT) as its first half; those rows of D1 hold W S,
+                // which the U epilogue has consumed by then.
+                const bool ok4 = __all_sync(0xffffffffu, mbar_wait(&bar[3], gi & 1, lim));
+                if (ok4) {
+                    tc_fence_after();
+                    const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024),
+                                      id_km, 1);
+                        umma_commit(&bar[4]);
+                    }
+                    __syncwarp();
+                } else {
+                    if (lane == 0) *abort_flag = 1;
+                    aborted = true;
+                    break;
+                }
+                continue;
+            }
+            bool ok = mbar_wait(&bar[b], (gi >> 1) & 1, lim);
+            don0 += ok && b == 0;
+            don1 += ok && b == 1;
             if (warp == 0 && __all_sync(0xffffffffu, ok)) {
-                // D_S = Mn S (critical), then D_O = [Mn(64..); Q'] S into buffer gi & 1
+                // D1[b] = [W; Q*Gam] S
                 tc_fence_after();
-                const uint64_t ad = sdesc_sw128(bufa + REC_MQ, 16, 1024);
-                const uint64_t bd = sdesc_sw128(base + C_S + sb * S_BYTES, DK * 128, 1024);
+                const uint64_t ad = sdesc_sw128(bufa + B_WQ, 16, 1024);
                 if (elect_one()) {
 #pragma unroll
                     for (int s = 0; s < DK / 16; ++s)
-                        umma_bf16(tmem, desc_add(ad, (s >> 2) * (MQ_ROWS * 128) + (s & 3) * 32),
-                                  desc_add(bd, s * 2048), idesc, s > 0);
-                    umma_commit(dS);
-                    if (!map) {
-#pragma unroll
-                        for (int s = 0; s < DK / 16; ++s)
-                            umma_bf16(tmem + 64 + 64 * (go & 1),
-                                      desc_add(ad, 64 * 128 + (s >> 2) * (MQ_ROWS * 128) + (s & 3) * 32),
-                                      desc_add(bd, s * 2048), idesc, s > 0);
-                        umma_commit(&dO[go & 1]);
-                    }
+                        umma_bf16(tmem + 32 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                                  desc_add(bd_s, s * 1024), id_km, s > 0);
+                    umma_commit(&bar[2]);
                 }
                 __syncwarp();
             }
-            if (out_thread && !map && ok) {
-                // outputs of the previous chunk: D_O + Y, off the critical path
-                if (cs > c_begin) {
-                    const uint32_t pb = (go - 1) & 1;
-                    ok = mbar_wait(&dO[pb], ((go - 1) >> 1) & 1, lim);
-                    tc_fence_after();
-                    if (ok) {
-                        float acc[32];
-                        tmem_ld32(tmem + 64 + 64 * pb + cl + lane_base, acc);
-                        tmem_ld_wait();
-                        const int64_t t = bos + (int64_t)(cs - 1 - cfirst) * C + (i - 64);
-                        if (t < eos) {
-                            uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+            if (warp < 2) {
+                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1).  While the
+                // product runs: this thread's row of Ut into registers, and the wait for the
+                // previous chunk's [x; P] U product, the last reader of the U image.
+                const int r = tid;
+                const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
+                float4 u4[8];
 #pragma unroll
-                            for (int k = 0; k < 4; ++k) {
-                                float yv[8], ov[8];
-                                unpack8(ycur[k], yv);
+                for (int j4 = 0; j4 < 8; ++j4)   // the M columns of a map see Ut = 0
+                    u4[j4] = mpart ? make_float4(0.f, 0.f, 0.f, 0.f) : ut[j4 ^ (r & 7)];
+                if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1, lim)) ok = false;
+                ok = ok && mbar_wait(&bar[2], gi & 1, lim);
+                tc_fence_after();
+                if (ok) {
+                    float acc[32];
+                    tmem_ld32(tmem + 32 * b + lane_base, acc);
+                    tmem_ld_wait();
 #pragma unroll
-                                for (int x = 0; x < 8; ++x) ov[x] = acc[8 * k + x] + yv[x];
-                                dst[k] = pack8(ov);
-                            }
-                        }
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        acc[4 * j4 + 0] = u4[j4].x - acc[4 * j4 + 0];
+                        acc[4 * j4 + 1] = u4[j4].y - acc[4 * j4 + 1];
+                        acc[4 * j4 + 2] = u4[j4].z - acc[4 * j4 + 2];
+                        acc[4 * j4 + 3] = u4[j4].w - acc[4 * j4 + 3];
                     }
+                    store_row_sw64(sm + C_UI, r, acc);
                 }
-                load_y(cs, ycur);
-            }
-            if (tid == 64) {
-                // the buffer of chunk cs - 1 takes chunk cs + 2 once both products of chunk
-                // cs - 1 have read it (D_O waited just above; a map item issues no D_O and
-                // its D_S was waited before the previous chunk's barrier)
-                if (ok && cs + 2 < c_end) issue_load(cs + 2, h, (gi + 2) % NBUF);
-                if (cs + kPrefetchAhead < c_end) {
-                    const uint8_t *r2 = rec_of(cs + kPrefetchAhead);
-                    bulk_prefetch_l2(r2 + REC_MQ, LOAD_BYTES);
-                    bulk_prefetch_l2(r2 + REC_B + blk * B_BLK, B_BLK);
-                    if (!map) bulk_prefetch_l2(r2 + REC_Y + blk * Y_BLK, Y_BLK);
+                fence_proxy_async();
+                tc_fence_before();
+                // the U image is complete: D2 = (K*Gam_C/Gam)^T U (only warps 0-1 wait here)
+                ok = bar_and(1, 64, ok);
+                if (warp == 0 && ok) {
+                    tc_fence_after();
+                    const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
+                    if (elect_one()) {
+#pragma unroll
+                        for (int s = 0; s < C / 16; ++s)
+                            umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
+                        umma_commit(&bar[3]);
+                    }
+                    __syncwarp();
+                }
+            } else {
+                // previous chunk's outputs, off the critical path; its [x; P] U product was
+                // the last reader of the other buffer, which then takes the next chunk
+                if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
+                if (tid == 64 && ok && cs + 1 < c_end) {
+                    chain_load(sm + (b ^ 1) * BUF_BYTES,
+                               records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES, blk,
+                               &bar[b ^ 1]);
+                    iss0 += b == 1;
+                    iss1 += b == 0;
+                }
+                // and the parts of the record kPrefetchAhead chunks on that this CTA reads
+                if (tid == 64 && cs + kPrefetchAhead < c_end) {
+                    const uint8_t *r2 = records + ((size_t)(cs + kPrefetchAhead - slot0) * H + h) * REC_BYTES;
+                    bulk_prefetch_l2(r2 + REC_WQ, REC_U - REC_WQ);
+                    bulk_prefetch_l2(r2 + REC_U + blk * 8192, 8192);
+                    bulk_prefetch_l2(r2 + REC_G, REC_BYTES - REC_G);
                 }
             }
-            // S <- Diag(Gam_C) S + D_S + B (row i, 32 columns)
-            ok = ok && mbar_wait(dS, gi & 1, lim);
+            // S <- Diag(Gam_C) S + D2 (row i = tid)
+            const float gc = reinterpret_cast<const float *>(buf + B_G)[i];
+            ok = mbar_wait(&bar[3], gi & 1, lim) && ok;
             tc_fence_after();
             if (ok) {
-                const float gc = reinterpret_cast<const float *>(sm + b * BUF_BYTES + REC_G)[i];
                 float acc[32];
-                tmem_ld32(tmem + cl + lane_base, acc);
+                tmem_ld32(D2 + lane_base, acc);
                 tmem_ld_wait();
-                uint8_t *img = sm + C_S + (sb ^ 1) * S_BYTES;
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    float bv[8], y[8];
-                    unpack8(bcur[k], bv);
-#pragma unroll
-                    for (int x = 0; x < 8; ++x) {
-                        S[8 * k + x] = gc * S[8 * k + x] + acc[8 * k + x] + bv[x];
-                        y[x] = S[8 * k + x];
-                    }
-                    *reinterpret_cast<uint4 *>(img + sw128_offset(i, cl + 8 * k, DK)) = pack8(y);
-                }
+                for (int j = 0; j < DVB; ++j) S[j] = gc * S[j] + acc[j];
+                store_row_sw64(sm + C_S, i, S);
             }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) bcur[k] = bnext[k];
-            if (!map) ++go;
             fence_proxy_async();
             tc_fence_before();
-            // S image complete, D_S and this chunk's record buffer read; the AND makes the
-            // decision to stop the same for every thread
-            if (!__syncthreads_and(ok && !*abort_flag)) {
-                ok = false;
+            // warps 0-3: S image complete and this chunk's record reads done; the AND makes
+            // the decision to stop the same for all of them
+            if (!bar_and(2, 128, ok && !*abort_flag)) {
+                if (tid == 0) *abort_flag = 1;
+                aborted = true;
                 break;
             }
         }
-        if (!ok) {
-            *abort_flag = 1;
+        if (aborted) {
             if (tid == 0) report(st, KDA_ERR_TIMEOUT, ((int64_t)n * H + h) * NBLK + blk, 11);
         } else {
             tc_fence_after();
-            if (out_thread && !map) {
-                // the item's last chunk
-                const uint32_t pb = (go - 1) & 1;
-                if (mbar_wait(&dO[pb], ((go - 1) >> 1) & 1, lim)) {
-                    tc_fence_after();
-                    float acc[32];
-                    tmem_ld32(tmem + 64 + 64 * pb + cl + lane_base, acc);
-                    tmem_ld_wait();
-                    const int64_t t = bos + (int64_t)(c_end - 1 - cfirst) * C + (i - 64);
-                    if (t < eos) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            float yv[8], ov[8];
-                            unpack8(ycur[k], yv);
-#pragma unroll
-                            for (int x = 0; x < 8; ++x) ov[x] = acc[8 * k + x] + yv[x];
-                            dst[k] = pack8(ov);
-                        }
-                    }
-                } else {
-                    *abort_flag = 1;
-                    report(st, KDA_ERR_TIMEOUT, ((int64_t)n * H + h) * NBLK + blk, 12);
-                }
-            }
+            bool ok_o = true;
+            if (warp >= 2 && warp < 4) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (!ok_o) *abort_flag = 1;
             // where the walk's end state goes: the running state, segment 1's start (first
             // pass, segment 0), the map, or nowhere (second pass, all but the last segment:
             // their ends are the next segments' composed starts)
@@ -1109,9 +1032,9 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 dst = sa.start + ((pairoff * sa.segs + 1) * DK + i) * DV + j0;
             else if (sa.mode == 2 && seg != s_eff - 1)
                 dst = nullptr;
-            if (dst) {
+            if (warp < 4 && dst) {
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)
+                for (int j4 = 0; j4 < DVB / 4; ++j4)
                     reinterpret_cast<float4 *>(dst)[j4] =
                         make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
             }
@@ -1119,34 +1042,29 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         tc_fence_before();
         __syncthreads();
     }
-    // After an expired wait: every product this CTA issued and every record load still in
-    // flight finishes (each wait bounded again) before the tensor memory is released.
-    if (*abort_flag) {
-        if (warp == 0) {
-            tc_fence_after();
-            if (elect_one()) umma_commit(drain);
-            __syncwarp();
-            mbar_wait(drain, 0, lim);
-        }
-        if (tid == 0) {
-            // a buffer holds at most one load that no wait has seen complete: its last one
-            for (int x = 0; x < NBUF; ++x)
-                if (ld_issued[x] > ld_done[x]) mbar_wait(&full[x], (ld_issued[x] - 1) & 1, lim);
-        }
-    }
     __syncthreads();
+    if (*abort_flag) {
+        // an expired wait: the products both issuing warps committed and the record loads
+        // still in flight finish (each wait bounded again) before the tensor memory is
+        // released and the CTA leaves
+        if (warp == 0 || warp == 4) {
+            tc_fence_after();
+            if (elect_one()) umma_commit(&bar[5]);
+            __syncwarp();
+        }
+        if (warp == 0) mbar_wait(&bar[5], 0, lim);
+        if (tid == 64) {   // a buffer holds at most one load no wait has seen: its last one
+            if (iss0 > don0) mbar_wait(&bar[0], (iss0 - 1) & 1, lim);
+            if (iss1 > don1) mbar_wait(&bar[1], (iss1 - 1) & 1, lim);
+        }
+        __syncthreads();
+    }
     if (warp == 0) {
         tc_fence_after();
-        tmem_dealloc(tmem, TMEM_COLS);
+        tmem_dealloc(tmem, 128);
     }
 }
 
-}  // namespace ac
-
-namespace c32 {
-constexpr int DVB = 32;          // value columns per item of the segment scan
-constexpr int DK_ROWS = DK;      // threads of the scan kernel (one per state row)
-constexpr int NBLK = DV / DVB;
 
 // The scan of the segment-parallel schedule: for every (sequence, head, 32-column block)
 // of the window, start(k + 1) = M_k start(k) + B_k for k = 1 .. s_eff - 2 (start(1) is
@@ -1214,6 +1132,294 @@ seg_scan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chun
 
 }  // namespace c32
 
+// ----------------------------------------------- chain kernel, all 128 columns
+namespace c128 {
+
+// One CTA per work item (sequence, head) owns all dv = 128 columns of S: the
+// products below are M = 128, N = 128, which cost the tensor core about as much
+// per instruction as N = 32, so one CTA does the work four narrower ones would.
+constexpr int CHAIN_THREADS = 512;
+constexpr uint32_t C_S = 0;                          // S image, MN-major SW128 [128 k][128 n]
+constexpr uint32_t C_UI = 32768;                     // U image, MN-major SW128 [64 k][128 n]
+constexpr uint32_t C_BUF0 = 49152;                   // record buffer 0 (REC_BYTES)
+constexpr uint32_t C_BAR = C_BUF0 + REC_BYTES;       // full[2], m1, m2, m3, drain; TMEM slot, flags
+constexpr uint32_t C_BUF1 = 140288;                  // record buffer 1
+constexpr uint32_t C_SMEM = C_BUF1 + REC_BYTES + 1024;
+static_assert(C_BAR + 72 <= C_BUF1 && C_BUF1 % 1024 == 0 && C_BUF0 % 1024 == 0,
+              "chain buffer layout");
+static_assert(REC_P % 1024 == 0 && REC_KT % 1024 == 0 && REC_U % 1024 == 0, "record alignment");
+static_assert(C_SMEM <= 232448, "chain kernel exceeds 227 KB of shared memory");
+
+__device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, uint64_t *full) {
+    mbar_arrive_expect_tx(full, REC_BYTES);
+    bulk_g2s(buf, rec, REC_BYTES, full);   // the whole record, one copy
+}
+
+// 32 fp32 values -> four 16-byte chunks of row r, columns j0.., of a 128B-swizzled
+// MN-major image whose 64-column groups are `rows` * 128 bytes apart
+__device__ __forceinline__ void store_row_sw128(uint8_t *img, int r, int j0, uint32_t rows,
+                                                const float (&x)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        float y[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) y[i] = x[8 * c8 + i];
+        *reinterpret_cast<uint4 *>(img + sw128_offset(r, j0 + 8 * c8, rows)) = pack8(y);
+    }
+}
+
+// Persistent over work items (sequence, head) of the sequences that own chunks in
+// the slot window [slot0, slot1); each item walks its chunks in order.  Warp w
+// holds lane quarter q = w & 3 and column block cb = w >> 2: thread (row 32q +
+// lane, columns 32cb..32cb+31) keeps its piece of S in registers (fp32), and S is
+// mirrored as the bf16 B operand image.  Per chunk, on the critical path:
+//   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
+//   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
+// ([x; P] reads the 64 rows in front of P as its first half; those rows of D1
+// hold W S, which has been consumed by then.)  D1 is double-buffered in TMEM so
+// that the output rows of chunk c (D1[64:128], lane quarters 2-3) are stored while
+// lane quarters 0-1 form U of chunk c+1.
+__global__ void __launch_bounds__(CHAIN_THREADS, 1)
+chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
+             int32_t slot0, int32_t slot1, const uint8_t *__restrict__ records,
+             const float *h0, float *__restrict__ state, __nv_bfloat16 *__restrict__ o,
+             StatusWord *st, Fault flt) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int32_t used = min(slot1, chunk_off[N]);
+    if (slot0 >= used) return;
+    const int n_first = slot_owner(chunk_off, N, slot0);
+    const int n_last = slot_owner(chunk_off, N, used - 1);
+    const int items = (n_last - n_first + 1) * H;
+    if ((int)blockIdx.x >= items) return;
+
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3, drain
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 48);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 52);
+    // record loads issued into / seen complete in buffers 0 and 1: kept in registers by
+    // thread 64, which issues every load (shared-memory counters beside the barriers
+    // measured 0.5 us a chunk slower)
+    uint32_t iss0 = 0, iss1 = 0, don0 = 0, don1 = 0;
+    const uint64_t lim = flt.wait_ns;
+    if (tid == 0) {
+        for (int x = 0; x < 6; ++x) mbar_init(&bar[x], 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const uint32_t D2 = tmem + 256;                    // D1 buffers at columns 0 and 128
+    const int q4 = warp & 3, cb = warp >> 2;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const uint32_t base = smem_u32(sm);
+    const uint32_t id_km = idesc_bf16(128, DV, false, true);   // A K-major, B MN-major
+    const uint32_t id_mm = idesc_bf16(128, DV, true, true);    // A MN-major, B MN-major
+    const uint64_t bd_s = sdesc_sw128(base + C_S, DK * 128, 1024);   // S image, K step 0
+    const uint64_t bd_u = sdesc_sw128(base + C_UI, C * 128, 1024);   // U image, K step 0
+    const int i = 32 * q4 + lane;   // this thread's state row
+    const int j0 = 32 * cb;         // and first column
+    uint32_t gi = 0;                // chunks processed by this CTA (drives buffer and barrier parity)
+    auto buf_off = [](uint32_t b) { return b ? C_BUF1 : C_BUF0; };
+
+    for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
+        const int h = item % H;
+        const int n = n_first + item / H;
+        const int32_t cfirst = chunk_off[n];
+        const int32_t c_begin = max(cfirst, slot0);
+        const int32_t c_end = min(chunk_off[n + 1], slot1);
+        if (c_begin >= c_end) continue;
+        const int64_t bos = cu[n];
+        const int64_t eos = cu[n + 1];
+        float S[32];
+        const int64_t soff = (((int64_t)n * H + h) * DK + i) * DV + j0;
+        float *srow = state + soff;
+        // the sequence's first chunk starts from h0 (zeros when absent), later windows from
+        // the running state
+        const float *s_in = c_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
+            S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
+        }
+        store_row_sw128(sm + C_S, i, j0, DK, S);
+        fence_proxy_async();
+        __syncthreads();
+        if (tid == 64 && !(item == (int)blockIdx.x && (int)blockIdx.x == flt.skip_cta)) {
+            chain_load(sm + buf_off(gi & 1),
+                       records + ((size_t)(c_begin - slot0) * H + h) * REC_BYTES, &bar[gi & 1]);
+            iss0 += (gi & 1) == 0;
+            iss1 += (gi & 1) == 1;
+        }
+
+        // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
+        // (lane quarters 2-3); waits for that chunk's [x; P] U product (barrier m3)
+        auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
+            const uint32_t pb = gprev & 1;
+            if (!mbar_wait(&bar[4], gprev & 1, lim)) return false;
+            tc_fence_after();
+            const int r = i - 64;
+            const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
+            float oacc[32];
+            tmem_ld32(tmem + 128 * pb + lane_base + j0, oacc);
+            tmem_ld_wait();
+            if (t < eos) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+#pragma unroll
+                for (int i8 = 0; i8 < 4; ++i8) {
+                    float y[8];
+#pragma unroll
+                    for (int x = 0; x < 8; ++x) y[x] = oacc[8 * i8 + x];
+                    dst[i8] = pack8(y);
+                }
+            }
+            return true;
+        };
+
+        for (int32_t cs = c_begin; cs < c_end; ++cs, ++gi) {
+            const uint32_t b = gi & 1;
+            uint8_t *buf = sm + buf_off(b);
+            const uint32_t bufa = base + buf_off(b);
+            bool ok = mbar_wait(&bar[b], (gi >> 1) & 1, lim);
+            don0 += ok && b == 0;
+            don1 += ok && b == 1;
+            if (warp == 0 && __all_sync(0xffffffffu, ok)) {
+                // D1[b] = [W; Q*Gam] S
+                tc_fence_after();
+                const uint64_t ad = sdesc_sw128(bufa + REC_WQ, 16, 1024);
+                if (elect_one()) {
+#pragma unroll
+                    for (int s = 0; s < DK / 16; ++s)
+                        umma_bf16(tmem + 128 * b, desc_add(ad, (s >> 2) * 16384 + (s & 3) * 32),
+                                  desc_add(bd_s, s * 2048), id_km, s > 0);
+                    umma_commit(&bar[2]);
+                }
+                __syncwarp();
+            }
+            if (q4 < 2) {
+                // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1)
+                ok = ok && mbar_wait(&bar[2], gi & 1, lim);
+                tc_fence_after();
+                if (ok) {
+                    const int r = i;
+                    float acc[32];
+                    tmem_ld32(tmem + 128 * b + lane_base + j0, acc);
+                    tmem_ld_wait();
+                    const float4 *ut = reinterpret_cast<const float4 *>(buf + REC_U + (cb * 64 + r) * 128);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 u4 = ut[j4 ^ (r & 7)];
+                        acc[4 * j4 + 0] = u4.x - acc[4 * j4 + 0];
+                        acc[4 * j4 + 1] = u4.y - acc[4 * j4 + 1];
+                        acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
+                        acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
+                    }
+                    store_row_sw128(sm + C_UI, r, j0, C, acc);
+                }
+            } else {
+                // previous chunk's outputs, off the critical path; its [x; P] U product was
+                // the last reader of the other buffer, which then takes the next chunk
+                if (cs > c_begin) ok = store_o(cs - 1, gi - 1) && ok;
+                if (tid == 64 && ok && cs + 1 < c_end) {
+                    chain_load(sm + buf_off(b ^ 1),
+                               records + ((size_t)(cs + 1 - slot0) * H + h) * REC_BYTES,
+                               &bar[b ^ 1]);
+                    iss0 += b == 1;
+                    iss1 += b == 0;
+                }
+                // and the record kPrefetchAhead chunks on
+                if (tid == 64 && cs + kPrefetchAhead < c_end)
+                    bulk_prefetch_l2(records + ((size_t)(cs + kPrefetchAhead - slot0) * H + h) * REC_BYTES,
+                                     REC_BYTES);
+            }
+            if (!ok) *abort_flag = 1;
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (*abort_flag) break;
+            if (warp == 0) {
+                tc_fence_after();
+                // D2 = (K*Gam_C/Gam)^T U  (on the recurrence) ...
+                const uint64_t akt = sdesc_sw128(bufa + REC_KT, C * 128, 1024);
+                const uint64_t azp = sdesc_sw128(bufa + REC_P - 8192, 16, 1024);
+                if (elect_one()) {
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 2048), id_mm, s > 0);
+                    umma_commit(&bar[3]);
+                    // ... then D1[b] += [x; P] U (outputs only), which runs while S is updated
+#pragma unroll
+                    for (int s = 0; s < C / 16; ++s)
+                        umma_bf16(tmem + 128 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 2048), id_km, 1);
+                    umma_commit(&bar[4]);
+                }
+                __syncwarp();
+            }
+            ok = mbar_wait(&bar[3], gi & 1, lim);
+            tc_fence_after();
+            if (ok) {
+                // S <- Diag(Gam_C) S + D2 (row i, columns j0..)
+                const float gc = reinterpret_cast<const float *>(buf + REC_G)[i];
+                float acc[32];
+                tmem_ld32(D2 + lane_base + j0, acc);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) S[j] = gc * S[j] + acc[j];
+                store_row_sw128(sm + C_S, i, j0, DK, S);
+            } else {
+                *abort_flag = 1;
+            }
+            fence_proxy_async();
+            tc_fence_before();
+            __syncthreads();
+            if (*abort_flag) break;
+        }
+        if (*abort_flag) {
+            if (tid == 0) report(st, KDA_ERR_TIMEOUT, (int64_t)n * H + h, 11);
+        } else {
+            tc_fence_after();
+            bool ok_o = true;
+            if (q4 >= 2) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (!ok_o) *abort_flag = 1;
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4)
+                reinterpret_cast<float4 *>(srow)[j4] =
+                    make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+    __syncthreads();
+    if (*abort_flag) {
+        // an expired wait: the issued products and the record loads still in flight finish
+        // (each wait bounded again) before the tensor memory is released
+        if (warp == 0) {
+            tc_fence_after();
+            if (elect_one()) umma_commit(&bar[5]);
+            __syncwarp();
+            mbar_wait(&bar[5], 0, lim);
+        }
+        if (tid == 64) {   // a buffer holds at most one load no wait has seen: its last one
+            if (iss0 > don0) mbar_wait(&bar[0], (iss0 - 1) & 1, lim);
+            if (iss1 > don1) mbar_wait(&bar[1], (iss1 - 1) & 1, lim);
+        }
+        __syncthreads();
+    }
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace c128
+
 }  // namespace tc
 
 size_t tc_record_bytes() { return tc::REC_BYTES; }
@@ -1253,10 +1459,6 @@ cudaError_t pipe_setup(int dev, Pipe *&out) {
     return e;
 }
 
-// Records: nbuf (1 or 2) buffers of `window` chunk slots x H records each.  With one
-// buffer the windows run prep, chain, prep, chain ... on `s`.  With two, prep of
-// window w + 1 runs beside chain of window w (see Pipe); the call's work is still
-// ordered after everything enqueued on `s` before it and before everything after it.
 // cuTensorMapEncodeTiled, reached through the runtime's entry-point query (the library
 // links no driver library)
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
@@ -1349,27 +1551,28 @@ cudaError_t kernel_attributes(int dev) {
     cudaError_t e = cudaFuncSetAttribute(tc::prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)tc::P_SMEM);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(tc::ac::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)tc::ac::C_SMEM);
+        e = cudaFuncSetAttribute(tc::c32::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::c32::C_SMEM);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(tc::c128::chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)tc::c128::C_SMEM);
     if (e == cudaSuccess) g_attr_set[dev] = true;
     return e;
 }
 
-// Test hook (kda_test_chain_fault): the next chain launch gets this wait limit and leaves
-// out the first record load of one CTA.
+// Test hook (kda_test_chain_fault): the next call's chain launches get this wait limit and
+// leave out the first record load of one CTA.
+constexpr uint64_t kWaitNs = 1000000000ull;   // the default limit of a bounded wait: 1 s
 std::mutex g_fault_mutex;
-tc::ac::Fault g_fault_next = {1000000000ull, -1};
+tc::Fault g_fault_next = {kWaitNs, -1};
 bool g_fault_armed = false;
 
-tc::ac::Fault take_fault() {
+tc::Fault take_fault() {
     std::lock_guard<std::mutex> lock(g_fault_mutex);
-    tc::ac::Fault f = g_fault_armed ? g_fault_next : tc::ac::Fault{1000000000ull, -1};
+    const tc::Fault f = g_fault_armed ? g_fault_next : tc::Fault{kWaitNs, -1};
     g_fault_armed = false;
     return f;
 }
-
-// Chain CTAs for a window of `seqs` sequences: one per item, at most one wave.
-int64_t chain_grid(int64_t items, int sm_count) { return std::min<int64_t>(items, sm_count); }
 
 }  // namespace
 
@@ -1390,7 +1593,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = kernel_attributes(dev);
     if (e != cudaSuccess) return e;
-    const ac::Fault flt = take_fault();
+    const Fault flt = take_fault();
     CUtensorMap tm[4];
     if (T_tot > 0) {
         const void *const ptrs[4] = {q, k, z, v};
@@ -1437,12 +1640,25 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
             if (e == cudaSuccess) e = cudaStreamWaitEvent(sc, P->prep_done[par], 0);
             if (e != cudaSuccess) return e;
         }
-        // a window holds at most min(N, window) sequences, each of H heads x 2 column blocks
-        const int64_t items = std::min<int64_t>(N, s1 - s0) * H * ac::NBLK;
+        // A window holds at most min(N, window) sequences.  While their 32-column items
+        // fit in about two waves the chain is latency-bound and the narrow kernel walks
+        // the chunks fastest; with more items the 128-column kernel, which does the same
+        // work in about half the SM time, finishes first.  Beside a prep kernel the
+        // narrow one is kept only while it leaves at least half of the SMs to the prep.
+        const int64_t seqs = std::min<int64_t>(N, s1 - s0);
+        const int64_t items32 = seqs * H * c32::NBLK;
         if (rec) rec->mark(sc);
-        ac::chain_kernel<<<(unsigned)chain_grid(items, sm_count), ac::THREADS, ac::C_SMEM, sc>>>(
-            cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run, (__nv_bfloat16 *)o,
-            st, SegArgs{0, 1, nullptr, nullptr}, flt);
+        if (items32 <= (piped ? (int64_t)sm_count / 2 : 2 * (int64_t)sm_count)) {
+            const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
+            c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, sc>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,
+                (__nv_bfloat16 *)o, st, SegArgs{0, 1, nullptr, nullptr}, flt);
+        } else {
+            const int64_t grid = std::min<int64_t>(seqs * H, sm_count);
+            c128::chain_kernel<<<(unsigned)grid, c128::CHAIN_THREADS, c128::C_SMEM, sc>>>(
+                cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,
+                (__nv_bfloat16 *)o, st, flt);
+        }
         if (rec) rec->mark(sc);
         if (piped) {
             e = cudaEventRecord(P->chain_done[par], sc);
@@ -1458,8 +1674,8 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
 }
 
 // The segment-parallel schedule (see SegArgs): per window of records, on `s` alone: prep,
-// first pass (segment 0 walked, later segments' maps), scan, second pass.  `start` and
-// `maps` hold N x H x segs blocks of the shapes in SegArgs.
+// first pass (segment 0 walked, later segments' maps), scan, second pass.  Always the
+// 32-column chain; `start` and `maps` hold N x H x segs blocks of the shapes in SegArgs.
 cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *v,
                                       const void *z, const void *beta, const float *A_log,
                                       const int32_t *cu, const int32_t *chunk_off, int N,
@@ -1475,7 +1691,7 @@ cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = kernel_attributes(dev);
     if (e != cudaSuccess) return e;
-    const ac::Fault flt = take_fault();
+    const Fault flt = take_fault();
     CUtensorMap tm[4];
     const void *const ptrs[4] = {q, k, z, v};
     e = tensor_maps(dev, ptrs, T_tot, H, tm);
@@ -1488,17 +1704,19 @@ cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *
             (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
             (int32_t)s0, records, st, tm[0], tm[1], tm[2], tm[3]);
         const int64_t pairs = std::min<int64_t>(N, s1 - s0) * H;
-        const int64_t items1 = pairs * (ac::NBLK + 2 * ac::NBLK * (segs - 1));
-        ac::chain_kernel<<<(unsigned)chain_grid(items1, sm_count), ac::THREADS, ac::C_SMEM, s>>>(
-            cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, h0, S_run, (__nv_bfloat16 *)o,
-            st, SegArgs{1, segs, start, maps}, flt);
+        const int64_t items1 = pairs * (c32::NBLK + 2 * c32::NBLK * (segs - 1));
+        c32::chain_kernel<<<(unsigned)std::min<int64_t>(items1, sm_count), c32::CHAIN_THREADS,
+                            c32::C_SMEM, s>>>(cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1,
+                                              records, h0, S_run, (__nv_bfloat16 *)o, st,
+                                              SegArgs{1, segs, start, maps}, flt);
         c32::seg_scan_kernel<<<(unsigned)std::min<int64_t>(pairs * c32::NBLK, 4 * sm_count),
                                c32::DK_ROWS, 0, s>>>(cu, chunk_off, N, H, (int32_t)s0,
                                                       (int32_t)s1, SegArgs{1, segs, start, maps});
-        const int64_t items2 = pairs * ac::NBLK * (segs - 1);
-        ac::chain_kernel<<<(unsigned)chain_grid(items2, sm_count), ac::THREADS, ac::C_SMEM, s>>>(
-            cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, records, h0, S_run, (__nv_bfloat16 *)o,
-            st, SegArgs{2, segs, start, maps}, flt);
+        const int64_t items2 = pairs * c32::NBLK * (segs - 1);
+        c32::chain_kernel<<<(unsigned)std::min<int64_t>(items2, sm_count), c32::CHAIN_THREADS,
+                            c32::C_SMEM, s>>>(cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1,
+                                              records, h0, S_run, (__nv_bfloat16 *)o, st,
+                                              SegArgs{2, segs, start, maps}, flt);
     }
     return cudaGetLastError();
 }
@@ -1511,7 +1729,7 @@ cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *
 extern "C" kda_status kda_test_chain_fault(int64_t wait_ns, int32_t skip_cta) {
     if (wait_ns <= 0) return KDA_ERR_INVALID_ARG;
     std::lock_guard<std::mutex> lock(kda::g_fault_mutex);
-    kda::g_fault_next = kda::tc::ac::Fault{(uint64_t)wait_ns, skip_cta};
+    kda::g_fault_next = kda::tc::Fault{(uint64_t)wait_ns, skip_cta};
     kda::g_fault_armed = true;
     return KDA_OK;
 }

@@ -87,8 +87,8 @@ size_t kda_chunk_fwd_workspace_size(int64_t total_tokens, int32_t num_seqs, int3
  * tiles (the chunkwise-parallel form of the dev.to page, section "The
  * Sequence Bottleneck").  The result equals the token-by-token recurrence
  * up to rounding.  On the tensor-core path, when a few long sequences would
- * leave most SMs idle (num_seqs x H x (2 + 4 (s - 1)) chain CTAs for s
- * segments fit in half of the device's SMs, with >= 64 chunks per segment of the
+ * leave most SMs idle (num_seqs x H x (4 + 8 (s - 1)) 32-column chain CTAs for s
+ * segments fit one wave of the device's SMs, with >= 64 chunks per segment of the
  * average sequence, s >= 2), the call runs the segment-parallel schedule of
  * kda_chunk_fwd_segmented with the largest such s <= 16, provided the workspace
  * holds its buffers (the size query includes them); otherwise the plain schedule.
@@ -212,7 +212,7 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
  * Limits: the problem must fit the array.  On the tensor-core path (bf16,
  * dk = dv = 128) the chunk plan ((num_seqs + 1) int32), the running state
  * (num_seqs * H * 64 KiB, only when final_state is NULL) and at least one
- * chunk record per head (H * 98,816 bytes) must fit in 32 MiB; larger
+ * chunk record per head (H * 90,624 bytes) must fit in 32 MiB; larger
  * problems are rejected with KDA_ERR_INVALID_ARG before anything is launched.
  * Fewer records fit than in a caller-sized workspace, so long inputs run in
  * more, smaller windows.
@@ -242,10 +242,10 @@ kda_status kda_chunk_fwd_noalloc(const void *q, const void *k, const void *v, co
  * limit `wait_ns` (nanoseconds, > 0; the default is one second) and leaves out
  * the first chunk-record load of chain CTA `skip_cta` (-1: none).  That CTA's
  * wait for the record then expires: the call reports KDA_ERR_TIMEOUT through
- * the status word (site 11), the CTA stops after letting every copy and
- * product it issued finish, and the library stays usable for the next call.
- * Returns KDA_ERR_INVALID_ARG for wait_ns <= 0.  Not thread-safe with respect
- * to which call picks the setting up; meant for tests only.
+ * the status word (info: the CTA's work item), the CTA stops after letting
+ * every copy and product it issued finish, and the library stays usable for
+ * the next call.  Returns KDA_ERR_INVALID_ARG for wait_ns <= 0.  Which call
+ * picks the setting up is not defined between threads; meant for tests only.
  */
 kda_status kda_test_chain_fault(int64_t wait_ns, int32_t skip_cta);
 

@@ -113,17 +113,21 @@ def test_tensor_core_path_bad_cu_seqlens_are_reported():
     assert torch.isfinite(o).all() and torch.isfinite(s).all()
 
 
-def test_expired_chain_wait_is_reported_and_the_next_call_is_clean():
+@pytest.mark.parametrize("lens", [[500, 300], [130, 257, 64, 3] * 4],
+                         ids=["32-column-chain", "128-column-chain"])
+def test_expired_chain_wait_is_reported_and_the_next_call_is_clean(lens):
     """The test hook leaves out the first record load of chain CTA 0 and gives every wait of
     the chain a 1 ms limit: that CTA's wait expires before it has issued any product, it
-    reports KDA_ERR_TIMEOUT (info = its item, sequence 0 / head 0 / column block 0), lets the
-    load it did issue finish and leaves.  The next call on the same workspace, without the
-    hook, matches the oracle."""
+    reports KDA_ERR_TIMEOUT (info = its first item, sequence 0 / head 0 / column block 0),
+    lets everything it issued finish and leaves.  The next call on the same workspace,
+    without the hook, matches the oracle."""
     from tests.gpu_util import TOL, score_prefill
-    d = inputs.make_prefill([500, 300], H=2, dk=128, dv=128, dtype="bf16", seed=50,
+    H = 2 if len(lens) == 2 else 32
+    d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=50 + len(lens),
                             h0_sigma=0.1, device=DEV)
-    T, H, dk = d["q"].shape
-    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, 2, H, dk, 128, torch.bfloat16),
+    T, _, dk = d["q"].shape
+    N = len(lens)
+    ws = kda.alloc_workspace(kda.chunk_fwd_workspace_size(T, N, H, dk, 128, torch.bfloat16),
                              DEV)
     lib = kda.load()
     assert lib.kda_test_chain_fault(1_000_000, 0) == kda.KDA_OK
@@ -133,5 +137,5 @@ def test_expired_chain_wait_is_reported_and_the_next_call_is_clean():
     assert code == kda.KDA_ERR_TIMEOUT and info == 0, (kda.status_string(code), info)
     o, hT = kda.chunk_fwd(d["q"], d["k"], d["v"], d["z"], d["beta"], d["A_log"],
                           d["cu_seqlens"], d["h0"], workspace=ws, check=True)
-    e_o, e_s = score_prefill(d, o, hT)
+    e_o, e_s = score_prefill(d, o, hT, heads=[0, H - 1])
     assert e_o <= TOL["bf16"] and e_s <= TOL["bf16"], (e_o, e_s)

@@ -117,13 +117,32 @@ def test_prefill_1m_workload():
     _score_whole(d, TOL["bf16"])
 
 
+def _chain_shape(N, H):
+    """Which chain kernel the library runs for N sequences of H heads (dk = dv = 128, bf16):
+    32-column items while N*H*4 fits in two waves of the device's SMs, else 128-column."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    return 32 if N * H * 4 <= 2 * sms else 128
+
+
+@pytest.mark.parametrize("z_shift", [-4.0, -6.0])
+@pytest.mark.parametrize("dtype,dk,dv", [("bf16", 128, 128), ("f32", 64, 64)])
+def test_long_memory_gates(z_shift, dtype, dk, dv):
+    """Gates near g = 0 keep the state for hundreds of tokens, so every chunk's output leans
+    on the state carried across many chunks (with the default gates it is forgotten within
+    a chunk); an error in the inter-chunk recurrence shows here."""
+    d = inputs.make_prefill([2000, 700, 65], H=4, dk=dk, dv=dv, dtype=dtype, seed=int(-z_shift),
+                            h0_sigma=0.1, z_shift=z_shift, device=DEV)
+    _run_and_score(d, dtype)
+
+
 @pytest.mark.parametrize("lens", [[130, 257], [130, 257, 64, 3] * 3],
-                         ids=["fewer-items-than-SMs", "CTAs-loop-over-items"])
-def test_chain_items(lens):
-    """The chain kernel (two 64-column CTAs per (sequence, head)) with initial states and
-    ragged chunks: 2 x 32 x 2 = 128 items (one each), and 12 x 32 x 2 = 768 items, more
-    than the SMs, so that each persistent CTA walks several items in turn."""
+                         ids=["few-seqs", "many-seqs"])
+def test_both_chain_shapes(lens):
+    """The narrow (32-column) and wide (128-column) chain kernels, with initial states and
+    ragged chunks; the two cases are chosen so that they select different kernels."""
     H = 32
+    shapes = {_chain_shape(len(l), H) for l in [[130, 257], [130, 257, 64, 3] * 3]}
+    assert shapes == {32, 128}
     d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=len(lens),
                             h0_sigma=0.1, device=DEV)
     _run_and_score(d, "bf16")

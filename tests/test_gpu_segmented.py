@@ -128,13 +128,12 @@ def test_nan_decay_is_reported_and_isolated():
 
 def _auto_segments(T, N, H):
     """The count kda_chunk_fwd picks by itself (include/kda.h): the largest s <= 16 whose
-    first pass, N H (2 + 4 (s - 1)) chain CTAs of 64 columns, fits in half of the SMs,
-    with >= 64 chunks per segment."""
+    first pass fits one wave of 32-column CTAs, with >= 64 chunks per segment."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     chunks = T // (64 * N)
     best = 1
     for s in range(2, 17):
-        if 2 * N * H * (2 + 4 * (s - 1)) > sms or chunks < 64 * s:
+        if N * H * (4 + 8 * (s - 1)) > sms or chunks < 64 * s:
             break
         best = s
     return best

@@ -30,7 +30,7 @@
 //   WQ  K-major [128 rows][128 K]: rows 0-63 W, rows 64-127 Q*Gam
 //   KT  MN-major [64 k-rows][128 m]: K*Gam_C/Gam, read as the M=dk x K=C operand
 //   P   K-major [64][64]
-//   Ut  fp32 [4 column blocks][64][32], float4 slot j4 of row r holds columns 4 (j4 ^ (r % 8))
+//   Ut  bf16 [4 column blocks][64][32], 16-byte piece j of row r holds columns 8 (j ^ ((r / 2) % 4))
 //   GC  fp32 [128] Gam_C
 #include <cuda.h>
 #include <string.h>
@@ -54,8 +54,16 @@ constexpr uint32_t REC_WQ = 0;
 constexpr uint32_t REC_KT = 32768;
 constexpr uint32_t REC_P = 49152;
 constexpr uint32_t REC_U = 57344;
-constexpr uint32_t REC_G = 90112;
-constexpr uint32_t REC_BYTES = 90624;
+constexpr uint32_t REC_G = 73728;
+constexpr uint32_t REC_BYTES = 74240;
+constexpr uint32_t UT_BLK = 64 * 32 * 2;   // bytes of one 32-column block of Ut (bf16)
+
+// Byte offset of the 16-byte piece j (columns 8j .. 8j+7) of row r in a 32-column block of
+// Ut: rows are 64 bytes, pieces swizzled so that 8 consecutive rows reading the same piece
+// hit 8 distinct 16-byte bank groups.
+__host__ __device__ __forceinline__ uint32_t ut_piece(uint32_t r, uint32_t j) {
+    return r * 64 + ((j ^ ((r >> 1) & 3)) << 4);
+}
 
 // ---------------------------------------------------------------- prep kernel
 constexpr int PREP_THREADS = 256;
@@ -87,7 +95,7 @@ constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewi
 constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], over the dead tables
 constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
 constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
-constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, fp32 [4][64][32]
+constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, bf16 [4][64][32]
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
 constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
 constexpr uint32_t P_SMEM = P_END + 1024;
@@ -97,7 +105,7 @@ static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "so
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
 static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
                   P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
-static_assert(P_WST + 16384 <= P_AS && P_UST + 32768 <= P_TB &&
+static_assert(P_WST + 16384 <= P_AS && P_UST + 16384 <= P_TB &&
                   P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
               "solve / epilogue staging overlaps live data");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
@@ -586,7 +594,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     //          lane quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut)
     //          x (32-column block), two 16-column TMEM loads in flight per wait.
     uint8_t *WST = sm + P_WST;   // [2 K halves][64 rows][128 B]
-    uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] fp32, slots swizzled
+    uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] bf16, pieces swizzled
     if ((warp & 3) < 2) {
         const int quarter = warp & 3;
         const int rr = 32 * quarter + lane;
@@ -607,13 +615,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                     *reinterpret_cast<uint4 *>(WST + sw128_offset(rr, 32 * cb + 8 * i8, 64)) = pack8(x);
                 }
             } else {
-                // row rr of column block cb; float4 j4 stored at slot j4 ^ (rr % 8) so that the
-                // chain kernel's row-per-thread reads hit distinct banks
-                float4 *dst = reinterpret_cast<float4 *>(UST + ((cb * 64 + rr) * 32) * 4);
+                // row rr of column block cb, bf16, pieces swizzled so that the chain
+                // kernels' row-per-thread reads hit distinct banks
+                uint8_t *dst = UST + cb * UT_BLK;
 #pragma unroll
-                for (int i4 = 0; i4 < 8; ++i4) {
-                    const float *v4 = i4 < 4 ? lo + 4 * i4 : hi + 4 * (i4 - 4);
-                    dst[i4 ^ (rr & 7)] = make_float4(v4[0], v4[1], v4[2], v4[3]);
+                for (int j = 0; j < 4; ++j) {
+                    float x[8];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) x[i] = j < 2 ? lo[8 * j + i] : hi[8 * (j - 2) + i];
+                    *reinterpret_cast<uint4 *>(dst + ut_piece(rr, j)) = pack8(x);
                 }
             }
         }
@@ -706,13 +716,13 @@ constexpr int NBLK = DV / DVB;
 constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x; P] U
 // a record buffer mirrors the record's first 57344 bytes (WQ, KT, P), then this CTA's U
 // block and Gam_C
-constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = 65536;
-constexpr uint32_t BUF_BYTES = 66560;
+constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = B_U + UT_BLK;
+constexpr uint32_t BUF_BYTES = (B_G + 512 + 1023) / 1024 * 1024;
 constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
 constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
 constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, m3, drain; TMEM slot, flags
 constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
-constexpr uint32_t LOAD_BYTES = REC_U + 8192 + 512;
+constexpr uint32_t LOAD_BYTES = REC_U + UT_BLK + 512;
 static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0 && B_P == REC_P && B_KT == REC_KT,
               "chain buffer layout");
 static_assert(C_S % 1024 == 0 && C_UI % 1024 == 0, "operand image alignment");
@@ -722,7 +732,7 @@ __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int
                                            uint64_t *full) {
     mbar_arrive_expect_tx(full, LOAD_BYTES);
     bulk_g2s(buf, rec, REC_U, full);   // WQ, KT, P in one copy
-    bulk_g2s(buf + B_U, rec + REC_U + blk * 8192, 8192, full);
+    bulk_g2s(buf + B_U, rec + REC_U + blk * UT_BLK, UT_BLK, full);
     bulk_g2s(buf + B_G, rec + REC_G, 512, full);
 }
 
@@ -938,11 +948,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 // product runs: this thread's row of Ut into registers, and the wait for the
                 // previous chunk's [x; P] U product, the last reader of the U image.
                 const int r = tid;
-                const float4 *ut = reinterpret_cast<const float4 *>(buf + B_U + r * 128);
-                float4 u4[8];
+                uint4 ur[4];
 #pragma unroll
-                for (int j4 = 0; j4 < 8; ++j4)   // the M columns of a map see Ut = 0
-                    u4[j4] = mpart ? make_float4(0.f, 0.f, 0.f, 0.f) : ut[j4 ^ (r & 7)];
+                for (int j = 0; j < 4; ++j)   // the M columns of a map see Ut = 0
+                    ur[j] = mpart ? make_uint4(0, 0, 0, 0)
+                                  : *reinterpret_cast<const uint4 *>(buf + B_U + ut_piece(r, j));
                 if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1, lim)) ok = false;
                 ok = ok && mbar_wait(&bar[2], gi & 1, lim);
                 tc_fence_after();
@@ -951,11 +961,11 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     tmem_ld32(tmem + 32 * b + lane_base, acc);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        acc[4 * j4 + 0] = u4[j4].x - acc[4 * j4 + 0];
-                        acc[4 * j4 + 1] = u4[j4].y - acc[4 * j4 + 1];
-                        acc[4 * j4 + 2] = u4[j4].z - acc[4 * j4 + 2];
-                        acc[4 * j4 + 3] = u4[j4].w - acc[4 * j4 + 3];
+                    for (int j = 0; j < 4; ++j) {
+                        float u[8];
+                        unpack8(ur[j], u);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) acc[8 * j + x] = u[x] - acc[8 * j + x];
                     }
                     store_row_sw64(sm + C_UI, r, acc);
                 }
@@ -989,7 +999,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 if (tid == 64 && cs + kPrefetchAhead < c_end) {
                     const uint8_t *r2 = records + ((size_t)(cs + kPrefetchAhead - slot0) * H + h) * REC_BYTES;
                     bulk_prefetch_l2(r2 + REC_WQ, REC_U - REC_WQ);
-                    bulk_prefetch_l2(r2 + REC_U + blk * 8192, 8192);
+                    bulk_prefetch_l2(r2 + REC_U + blk * UT_BLK, UT_BLK);
                     bulk_prefetch_l2(r2 + REC_G, REC_BYTES - REC_G);
                 }
             }
@@ -1143,7 +1153,7 @@ constexpr uint32_t C_S = 0;                          // S image, MN-major SW128 
 constexpr uint32_t C_UI = 32768;                     // U image, MN-major SW128 [64 k][128 n]
 constexpr uint32_t C_BUF0 = 49152;                   // record buffer 0 (REC_BYTES)
 constexpr uint32_t C_BAR = C_BUF0 + REC_BYTES;       // full[2], m1, m2, m3, drain; TMEM slot, flags
-constexpr uint32_t C_BUF1 = 140288;                  // record buffer 1
+constexpr uint32_t C_BUF1 = (C_BAR + 72 + 1023) / 1024 * 1024;   // record buffer 1
 constexpr uint32_t C_SMEM = C_BUF1 + REC_BYTES + 1024;
 static_assert(C_BAR + 72 <= C_BUF1 && C_BUF1 % 1024 == 0 && C_BUF0 % 1024 == 0,
               "chain buffer layout");
@@ -1312,14 +1322,13 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     float acc[32];
                     tmem_ld32(tmem + 128 * b + lane_base + j0, acc);
                     tmem_ld_wait();
-                    const float4 *ut = reinterpret_cast<const float4 *>(buf + REC_U + (cb * 64 + r) * 128);
+                    const uint8_t *ut = buf + REC_U + cb * UT_BLK;
 #pragma unroll
-                    for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 u4 = ut[j4 ^ (r & 7)];
-                        acc[4 * j4 + 0] = u4.x - acc[4 * j4 + 0];
-                        acc[4 * j4 + 1] = u4.y - acc[4 * j4 + 1];
-                        acc[4 * j4 + 2] = u4.z - acc[4 * j4 + 2];
-                        acc[4 * j4 + 3] = u4.w - acc[4 * j4 + 3];
+                    for (int j = 0; j < 4; ++j) {
+                        float u[8];
+                        unpack8(*reinterpret_cast<const uint4 *>(ut + ut_piece(r, j)), u);
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) acc[8 * j + x] = u[x] - acc[8 * j + x];
                     }
                     store_row_sw128(sm + C_UI, r, j0, C, acc);
                 }

@@ -212,7 +212,7 @@ kda_status kda_chunk_fwd_profiled(const void *q, const void *k, const void *v, c
  * Limits: the problem must fit the array.  On the tensor-core path (bf16,
  * dk = dv = 128) the chunk plan ((num_seqs + 1) int32), the running state
  * (num_seqs * H * 64 KiB, only when final_state is NULL) and at least one
- * chunk record per head (H * 90,624 bytes) must fit in 32 MiB; larger
+ * chunk record per head (H * 74,240 bytes) must fit in 32 MiB; larger
  * problems are rejected with KDA_ERR_INVALID_ARG before anything is launched.
  * Fewer records fit than in a caller-sized workspace, so long inputs run in
  * more, smaller windows.

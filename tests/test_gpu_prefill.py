@@ -163,10 +163,10 @@ def test_profiled_entry_pairs_and_stream_order():
     results as kda_chunk_fwd; inputs written on a side stream just before the call, and
     outputs read on it right after, see the call's work in order (the call may run
     kernels on the library's own streams)."""
-    # more than one window of chunk records (1 GiB), so that the double-buffered schedule
-    # with its own streams runs
+    # more than one window of chunk records (1 GiB: 451 chunk slots of 32 heads), so that
+    # the double-buffered schedule with its own streams runs
     # (the empty sequence in the middle owns no chunk: its final state is its initial one)
-    d = inputs.make_prefill([20000, 0, 4000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
+    d = inputs.make_prefill([26000, 0, 8000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
                             h0_sigma=0.1, device=DEV)
     T, H, dk = d["q"].shape
     N = 3

@@ -69,7 +69,8 @@ def test_two_calls_in_a_row_match_the_workspace_entry():
     _check_against_workspace_entry(d1, "bf16")
     # second call, right after: a longer sequence that needs several windows of the
     # fixed scratch (more heads, fewer records fit), no initial state
-    d2 = inputs.make_prefill([3000], H=8, dk=128, dv=128, dtype="bf16", seed=42, device=DEV)
+    # (8 heads: 56 chunk slots of records fit the array, the sequence has 79)
+    d2 = inputs.make_prefill([5000], H=8, dk=128, dv=128, dtype="bf16", seed=42, device=DEV)
     _check_against_workspace_entry(d2, "bf16")
 
 
@@ -101,8 +102,8 @@ def test_cuda_core_path_in_place():
 def test_too_large_is_refused_before_launch():
     lib = kda.load()
     fake = [ctypes.c_void_p(0x10000 * (i + 1)) for i in range(10)]
-    # one record per head no longer fits 32 MiB at H = 400
-    rc = lib.kda_chunk_fwd_noalloc(*fake[:7], 1, 64, 400, 128, 128, kda.KDA_BF16, None,
+    # one record per head (74,240 bytes) no longer fits 32 MiB at H = 500
+    rc = lib.kda_chunk_fwd_noalloc(*fake[:7], 1, 64, 500, 128, 128, kda.KDA_BF16, None,
                                    fake[7], fake[8], None, None)
     assert rc == kda.KDA_ERR_INVALID_ARG
     # the running state of 64 x 32 heads (128 MiB) does not fit when final_state is NULL

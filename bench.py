@@ -356,7 +356,7 @@ def run_ours(args, rank, world, local):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
     pk, pk_src = peaks()
-    head, d = prefill_leg(HEADLINE, dev, stream, args.steps, args.warmup, world, pk, pk_src,
+    head, d = prefill_leg(args.workload, dev, stream, args.steps, args.warmup, world, pk, pk_src,
                           clock=True, keep=True)
     line = {
         "metric": METRIC, "value": head["value"], "unit": "tokens/s", "n_gpus": world,
@@ -369,13 +369,13 @@ def run_ours(args, rank, world, local):
     if not args.no_e2e:
         line["e2e"] = e2e_bench(args, d, dev, stream, world)
     sample = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and args.workload == HEADLINE:
         sample = host_prefix(d, CPU_SAMPLE_MAX)
     del d
     torch.cuda.empty_cache()
     if not args.headline_only:
         line["workloads"] = {}
-        for name in EXTRA_PREFILL:
+        for name in [w for w in EXTRA_PREFILL if w != args.workload]:
             res, _ = prefill_leg(name, dev, stream, args.steps, args.warmup, world, pk, pk_src)
             line["workloads"][name] = res
         if not args.no_decode:
@@ -674,6 +674,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--headline-only", action="store_true",
                     help="time the headline workload (and e2e / CPU baseline) only")
+    ap.add_argument("--workload", default=HEADLINE,
+                    help="prefill workload of the line (default: the headline, prefill_1m); "
+                         "another name from inputs.WORKLOADS is for inspection and profiles")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

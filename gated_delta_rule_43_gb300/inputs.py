@@ -65,6 +65,12 @@ WORKLOADS = {
     "prefill_1m": Workload(
         "prefill_1m", "prefill", H=16, dk=128, dv=128, dtype="bf16", seed=4,
         seqlens=(1048576,), notes="B=1, T=1,048,576, bf16, carried state, final state"),
+    # a smaller packed case of the varlen recipe, for kernel profiles that must hold only a
+    # few GB on the device (the 128-column chain kernel runs on it as on varlen_64)
+    "varlen_16": Workload(
+        "varlen_16", "prefill", H=32, dk=128, dv=128, dtype="bf16", seed=5,
+        seqlens=("uniform", 16, 512, 4096), h0_sigma=0.1,
+        notes="16 packed sequences, lengths U[512, 4096], initial state N(0, 0.01)"),
 }
 
 

@@ -47,4 +47,4 @@ def test_decode_stream():
     assert x["q"].shape == (4, 2, 16) and x["v"].shape == (4, 2, 8) and x["beta"].shape == (4, 2)
     assert s.state0.shape == (4, 2, 16, 8)
     assert set(inputs.WORKLOADS) == {"tiny_fp32", "prefill_8k", "varlen_64", "decode_256",
-                                     "prefill_1m"}
+                                     "prefill_1m", "varlen_16"}

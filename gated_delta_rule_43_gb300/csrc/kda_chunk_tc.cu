@@ -233,7 +233,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 
     // ---- (A) gate into the fp32 G scratch (row-wise, 16-byte stores), then the in-tile
     //          inclusive cumsums down the columns: thread (tile, channel) walks its 16 rows,
-    //          leaves G in place, records the tile sum and checks the range
+    //          leaves G in place, records the tile sum and checks the range.  Every g lies in
+    //          [g_min, 0] (NaN aside), so a tile's cumulative decay falls monotonically from 0
+    //          and stays in [-80, 0] iff its last value does; a NaN reaches the last value
+    //          too.  Only a tile whose last value fails is searched for its first bad row.
     float *GS = reinterpret_cast<float *>(sm + P_G);
 #pragma unroll
     for (int u = 0; u < NU; ++u) {
@@ -253,15 +256,18 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const int ta = e >> 7, c = e & (DK - 1);
         float *col = GS + (16 * ta) * GLD + c;
         float run = 0.f;
-        int bad_row = -1;
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             run += col[i * GLD];
             col[i * GLD] = run;
-            bad_row = (bad_row < 0 && 16 * ta + i < L && !decay_ok(run)) ? 16 * ta + i : bad_row;
         }
         TOT[ta * DK + c] = run;
-        if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
+        if (!decay_ok(run)) {
+            int bad_row = -1;
+            for (int i = 0; i < 16 && bad_row < 0; ++i)
+                if (16 * ta + i < L && !decay_ok(col[i * GLD])) bad_row = 16 * ta + i;
+            if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
+        }
     }
     __syncthreads();
     // this thread's G values and k, q chunks, read before pass B reuses their space
@@ -282,24 +288,25 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tmem_relinquish();
         tc_fence_before();
     }
-    // tile references, Gam_C and the per-(tile, channel) factor tables
+    // tile references, Gam_C and the per-(tile, channel) factor tables (fast exponentials:
+    // arguments down to -320 lose < 3e-5 of relative precision in their scaling by log2 e)
     if (tid < DK) {
         const int c = tid;
         float run = 0.f, ref[4];
 #pragma unroll
         for (int t = 0; t < 4; ++t) {
             ref[t] = run;
-            ER[t * DK + c] = expf(run);
+            ER[t * DK + c] = __expf(run);
             run += TOT[t * DK + c];
         }
-        *reinterpret_cast<float *>(rec + REC_G + 4 * c) = expf(run);
+        *reinterpret_cast<float *>(rec + REC_G + 4 * c) = __expf(run);
 #pragma unroll
-        for (int t = 0; t < 4; ++t) KTF[t * DK + c] = expf(run - ref[t]);
+        for (int t = 0; t < 4; ++t) KTF[t * DK + c] = __expf(run - ref[t]);
         int p = 0;
 #pragma unroll
         for (int a2 = 1; a2 < 4; ++a2)
 #pragma unroll
-            for (int b = 0; b < a2; ++b, ++p) RT[p * DK + c] = expf(ref[a2] - ref[b]);
+            for (int b = 0; b < a2; ++b, ++p) RT[p * DK + c] = __expf(ref[a2] - ref[b]);
     }
     __syncthreads();
 

@@ -88,7 +88,8 @@ constexpr uint32_t KC_ROWS = 160;       //   image a = rows 8a(a+1) .. 8a(a+1) +
 constexpr uint32_t P_KGV = 13312;       // (after the A/P products) MN-major [64][256]: K*Gam | V
 constexpr uint32_t P_AS = 46080;        //   fp32 A [64][68]
 constexpr uint32_t P_TS = 63488;        //   fp32 T [64][68]
-constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][16] N^2 / N^3 blocks
+constexpr uint32_t P_XS = 80896;        //   fp32 [4][16][XLD] N^2 / N^3 blocks
+constexpr int XLD = 20;                 //   padded row stride: conflict-free row-wise reads
 constexpr uint32_t P_ZT = 47104;        // (until pass A) z tile, TMA, [2][64][128 B] swizzled
 constexpr uint32_t P_KT = 63488;        // (until the table pass) k tile, likewise
 constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewise
@@ -101,7 +102,7 @@ constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored
 constexpr uint32_t P_SMEM = P_END + 1024;
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
-static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * 16 * 4 <= P_TB, "solve scratch");
+static_assert(P_TS + 64 * LDA * 4 <= P_XS && P_XS + 4 * 16 * XLD * 4 <= P_TB, "solve scratch");
 static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) image");
 static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
                   P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
@@ -524,15 +525,15 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             acc16(x, nrow(4, i), ncol(0, jq), LDA);
             acc16(x, nrow(2, i), ncol(3, jq), LDA);
         }
-        *reinterpret_cast<float4 *>(XS + q * 256 + i * 16 + 4 * jq) = x;
+        *reinterpret_cast<float4 *>(XS + q * 16 * XLD + i * XLD + 4 * jq) = x;
     }
     if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
     __syncthreads();
     if (tid < 64) {  // N^3_30 = N32 N^2_20
         const int i = tid >> 2, jq = tid & 3;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        acc16(x, nrow(2, i), XS + 4 * jq, 16);
-        *reinterpret_cast<float4 *>(XS + 3 * 256 + i * 16 + 4 * jq) = x;
+        acc16(x, nrow(2, i), XS + 4 * jq, XLD);
+        *reinterpret_cast<float4 *>(XS + 3 * 16 * XLD + i * XLD + 4 * jq) = x;
     } else if (tid < 64 + 192) {
         // zero blocks (a, b > a): (0,1) (0,2) (0,3) (1,2) (1,3) (2,3), 16 rows x two 16-byte chunks
         const int e = tid - 64, ub = e >> 5, rc = e & 31;
@@ -556,11 +557,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             for (int t = 0; t < 16; ++t) mrow[t] = -nr[t];
             if (n2 >= 0) {
 #pragma unroll
-                for (int t = 0; t < 16; ++t) mrow[t] += XS[n2 * 256 + i * 16 + t];
+                for (int t = 0; t < 16; ++t) mrow[t] += XS[n2 * 16 * XLD + i * XLD + t];
             }
             if (n2 == 2) {
 #pragma unroll
-                for (int t = 0; t < 16; ++t) mrow[t] -= XS[3 * 256 + i * 16 + t];
+                for (int t = 0; t < 16; ++t) mrow[t] -= XS[3 * 16 * XLD + i * XLD + t];
             }
             float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
             acc16(x, mrow, TS + (16 * b) * LDA + 16 * b + 4 * jq, LDA);

@@ -743,8 +743,8 @@ constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x;
 constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = B_U + UT_BLK;
 constexpr uint32_t BUF_BYTES = (B_G + 512 + 1023) / 1024 * 1024;
 constexpr uint32_t C_S = 2 * BUF_BYTES;              // S image, MN-major 64B-swizzle [128 k][32 n]
-constexpr uint32_t C_UI = C_S + 8192;                // U image, MN-major 64B-swizzle [64 k][32 n]
-constexpr uint32_t C_BAR = C_UI + 4096;              // full[2], m1, m2, m3, drain; TMEM slot, flags
+constexpr uint32_t C_UI = C_S + 8192;                // U images of even / odd chunks, MN-major 64B-swizzle [64 k][32 n]
+constexpr uint32_t C_BAR = C_UI + 8192;              // full[2], m1, m2, m3, drain, d2i; TMEM slot, flag
 constexpr uint32_t C_SMEM = C_BAR + 128 + 1024;
 constexpr uint32_t LOAD_BYTES = REC_U + UT_BLK + 512;
 static_assert(B_G + 512 <= BUF_BYTES && BUF_BYTES % 1024 == 0 && B_P == REC_P && B_KT == REC_KT,
@@ -801,9 +801,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const int items = (n_last - n_first + 1) * H * ipp;
     if ((int)blockIdx.x >= items) return;
 
-    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);  // full0, full1, m1, m2, m3, drain
-    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 48);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 52);
+    // full0, full1, m1 (D1), m2 (D2), m3 ([x; P] U), drain, d2i (D2 issued)
+    uint64_t *bar = reinterpret_cast<uint64_t *>(sm + C_BAR);
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + C_BAR + 56);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C_BAR + 60);
     // record loads issued into / seen complete in buffers 0 and 1: kept in registers by
     // thread 64, which issues every load (shared-memory counters beside the barriers
     // measured 0.5 us a chunk slower)
@@ -812,6 +813,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     if (tid == 0) {
         for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
         mbar_init(&bar[5], 2);   // one commit from each issuing warp (0 and 4)
+        mbar_init(&bar[6], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -829,7 +831,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const uint32_t id_km = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
     const uint32_t id_mm = idesc_bf16(128, DVB, true, true);    // A MN-major, B MN-major
     const uint64_t bd_s = sdesc_sw64(base + C_S, 128 * 64, 512);    // S image, K step 0
-    const uint64_t bd_u = sdesc_sw64(base + C_UI, 64 * 64, 512);    // U image, K step 0
+    const uint64_t bd_u = sdesc_sw64(base + C_UI, 64 * 64, 512);    // U image 0, K step 0
     const int i = tid;  // this thread's state row
     uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
@@ -928,19 +930,20 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             uint8_t *buf = sm + b * BUF_BYTES;
             const uint32_t bufa = base + b * BUF_BYTES;
             if (warp == 4) {
-                // D1[b] += [x; P] U (outputs only), issued behind D2 so that it runs while S is
-                // updated; warp 4 joins no per-chunk barrier.  [x; P] reads the 64 rows in
-                // front of P (the tail of KT) as its first half; those rows of D1 hold W S,
-                // which the U epilogue has consumed by then.
-                const bool ok4 = __all_sync(0xffffffffu, mbar_wait(&bar[3], gi & 1, lim));
+                // D1[b] += [x; P] U (outputs only), issued as soon as D2 has been: the
+                // in-order tensor pipe runs it right behind D2, while S is updated and well
+                // before the next D1.  Warp 4 joins no per-chunk barrier.  [x; P] reads the
+                // 64 rows in front of P (the tail of KT) as its first half; those rows of D1
+                // hold W S, which the U epilogue has consumed by then.
+                const bool ok4 = __all_sync(0xffffffffu, mbar_wait(&bar[6], gi & 1, lim));
                 if (ok4) {
                     tc_fence_after();
                     const uint64_t azp = sdesc_sw128(bufa + B_P - 8192, 16, 1024);
                     if (elect_one()) {
 #pragma unroll
                         for (int s = 0; s < C / 16; ++s)
-                            umma_bf16(tmem + 32 * b, desc_add(azp, s * 32), desc_add(bd_u, s * 1024),
-                                      id_km, 1);
+                            umma_bf16(tmem + 32 * b, desc_add(azp, s * 32),
+                                      desc_add(bd_u, b * 4096 + s * 1024), id_km, 1);
                         umma_commit(&bar[4]);
                     }
                     __syncwarp();
@@ -969,15 +972,15 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             }
             if (warp < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1).  While the
-                // product runs: this thread's row of Ut into registers, and the wait for the
-                // previous chunk's [x; P] U product, the last reader of the U image.
+                // product runs: this thread's row of Ut into registers.  The U image of this
+                // parity was last read two chunks ago, by products the outputs of the
+                // previous chunk waited for.
                 const int r = tid;
                 uint4 ur[4];
 #pragma unroll
                 for (int j = 0; j < 4; ++j)   // the M columns of a map see Ut = 0
                     ur[j] = mpart ? make_uint4(0, 0, 0, 0)
                                   : *reinterpret_cast<const uint4 *>(buf + B_U + ut_piece(r, j));
-                if (cs > c_begin && !mbar_wait(&bar[4], (gi - 1) & 1, lim)) ok = false;
                 ok = ok && mbar_wait(&bar[2], gi & 1, lim);
                 tc_fence_after();
                 if (ok) {
@@ -991,7 +994,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
 #pragma unroll
                         for (int x = 0; x < 8; ++x) acc[8 * j + x] = u[x] - acc[8 * j + x];
                     }
-                    store_row_sw64(sm + C_UI, r, acc);
+                    store_row_sw64(sm + C_UI + b * 4096, r, acc);
                 }
                 fence_proxy_async();
                 tc_fence_before();
@@ -1003,8 +1006,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                     if (elect_one()) {
 #pragma unroll
                         for (int s = 0; s < C / 16; ++s)
-                            umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, s * 1024), id_mm, s > 0);
+                            umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, b * 4096 + s * 1024),
+                                      id_mm, s > 0);
                         umma_commit(&bar[3]);
+                        mbar_arrive(&bar[6]);   // warp 4 may queue [x; P] U behind D2
                     }
                     __syncwarp();
                 }

@@ -154,6 +154,24 @@ __device__ __forceinline__ float rcp_approx(float x) {
 // e^x as 2^(x log2 e); results below the normal range flush to 0
 __device__ __forceinline__ float exp_decay(float x) { return ex2_approx(x * kLog2e); }
 
+// Per-channel fp32 rows in shared memory (the gate scratch and the factor tables) keep
+// channel c = 64 h + 8 j + 4 g + e (h, g in {0, 1}, j < 8, e < 4) at position
+// 64 h + 32 g + 4 j + e, so that the 8 lanes reading channels 64 h + 8 j .. + 7 for
+// j = 0..7 read two contiguous 128-byte lines.
+__host__ __device__ __forceinline__ int chan_pos(int c) {
+    return (c & 64) + ((c & 4) << 3) + ((c >> 1) & 28) + (c & 3);
+}
+__host__ __device__ __forceinline__ int pos_chan(int p) {
+    return (p & 64) + ((p & 28) << 1) + ((p >> 3) & 4) + (p & 3);
+}
+// the 8 values of channels c .. c + 7 (c a multiple of 8) from a position-ordered row
+__device__ __forceinline__ void ld8p(const float *row, int c, float (&x)[8]) {
+    const int p = chan_pos(c);
+    const float4 a = *reinterpret_cast<const float4 *>(row + p);
+    const float4 b = *reinterpret_cast<const float4 *>(row + p + 32);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+
 // chunk slot -> (sequence, first token, valid rows); false when the slot is unused
 __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chunk_off, int N,
                                            int32_t slot, int &n, int64_t &t0, int &L) {
@@ -232,12 +250,13 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tma_load_3d(sm + P_QT + 8192, &tmap_q, 64, h, (int32_t)t0, kqbar);
     }
 
-    // Row-wise element passes: thread (row-in-tile rl, 8-channel chunk ch) owns unit u =
-    // row 16u + rl of tile u, u = 0..3, so that every thread writes the same number of
-    // column-scaled key images (tile a's rows appear in images a..3).
-    const int rl = lane & 15;
-    const int ch = 2 * warp + (lane >> 4);
-    const int c = 8 * ch;
+    // Row-wise element passes: thread (row-in-tile rl, 8-channel chunk c .. c + 7) owns
+    // unit u = row 16u + rl of tile u, u = 0..3, so that every thread writes the same
+    // number of column-scaled key images (tile a's rows appear in images a..3).  A warp
+    // covers 4 rows x 64 channels (one 128-byte line of each row of a K half): its
+    // 16-byte stores fill whole lines, in shared and in global memory.
+    const int rl = 4 * (warp & 3) + (lane >> 3);
+    const int c = 64 * (warp >> 2) + 8 * (lane & 7);
     const float alog = A_log[h];
     const float beta_v = tid < L ? __bfloat162float(beta[(t0 + min(tid, C - 1)) * H + h]) : 0.f;
     const float nl2e = -expf(alog) * kLog2e;   // -e^A log2(e)
@@ -264,13 +283,13 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
         for (int i = 0; i < 8; ++i)
             zz[i] = r < L ? kGMin * rcp_approx(1.0f + ex2_approx(nl2e * zz[i])) : 0.f;
-        float4 *dst = reinterpret_cast<float4 *>(GS + r * GLD + c);
-        dst[0] = make_float4(zz[0], zz[1], zz[2], zz[3]);
-        dst[1] = make_float4(zz[4], zz[5], zz[6], zz[7]);
+        float *dst = GS + r * GLD + chan_pos(c);
+        *reinterpret_cast<float4 *>(dst) = make_float4(zz[0], zz[1], zz[2], zz[3]);
+        *reinterpret_cast<float4 *>(dst + 32) = make_float4(zz[4], zz[5], zz[6], zz[7]);
     }
     __syncthreads();
 #pragma unroll
-    for (int e = tid; e < 4 * DK; e += PREP_THREADS) {
+    for (int e = tid; e < 4 * DK; e += PREP_THREADS) {   // (tile, position) pairs
         const int ta = e >> 7, c = e & (DK - 1);
         float *col = GS + (16 * ta) * GLD + c;
         float run = 0.f;
@@ -291,7 +310,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // this thread's G values and k, q chunks, read before pass B reuses their space
     float trun[NU][8];
 #pragma unroll
-    for (int u = 0; u < NU; ++u) ld8(GS + (16 * u + rl) * GLD + c, trun[u]);
+    for (int u = 0; u < NU; ++u) ld8p(GS + (16 * u + rl) * GLD, c, trun[u]);
     ok = mbar_wait(kqbar, 0) && ok;
     uint4 kraw[NU], qraw[NU];
 #pragma unroll
@@ -306,7 +325,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tmem_relinquish();
         tc_fence_before();
     }
-    // tile references, Gam_C and the per-(tile, channel) factor tables
+    // tile references, Gam_C and the per-(tile, channel) factor tables (thread = position)
     if (tid < DK) {
         const int c = tid;
         float run = 0.f, ref[4];
@@ -316,7 +335,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             ER[t * DK + c] = exp_decay(run);
             run += TOT[t * DK + c];
         }
-        *reinterpret_cast<float *>(rec + REC_G + 4 * c) = exp_decay(run);
+        *reinterpret_cast<float *>(rec + REC_G + 4 * pos_chan(c)) = exp_decay(run);
 #pragma unroll
         for (int t = 0; t < 4; ++t) KTF[t * DK + c] = exp_decay(run - ref[t]);
         int p = 0;
@@ -336,8 +355,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         float kk[8], qq[8], er[8], ktf[8];
         unpack8(kraw[u], kk);
         unpack8(qraw[u], qq);
-        ld8(ER + a * DK + c, er);
-        ld8(KTF + a * DK + c, ktf);
+        ld8p(ER + a * DK, c, er);
+        ld8p(KTF + a * DK, c, ktf);
         float kr[8], qr[8], kf[8], qg[8], kt[8], kg[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -363,7 +382,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
         for (int a2 = a + 1; a2 < 4; ++a2) {
             float rt[8], x[8];
-            ld8(RT + ((a2 * (a2 - 1)) / 2 + a) * DK + c, rt);
+            ld8p(RT + ((a2 * (a2 - 1)) / 2 + a) * DK, c, rt);
 #pragma unroll
             for (int i = 0; i < 8; ++i) x[i] = kf[i] * rt[i];
             *reinterpret_cast<uint4 *>(sm + P_KC + sw128_offset(8 * a2 * (a2 + 1) + r, c, KC_ROWS)) = pack8(x);

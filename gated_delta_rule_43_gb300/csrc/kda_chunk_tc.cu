@@ -200,39 +200,24 @@ __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
             const __nv_bfloat16 *__restrict__ beta, const float *__restrict__ A_log,
-            const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N, int H,
-            int32_t slot0, uint8_t *__restrict__ records, StatusWord *st,
+            const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_off, int N,
+            int64_t T_tot, int H, int32_t slot0, uint8_t *__restrict__ records, StatusWord *st,
             const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
             const __grid_constant__ CUtensorMap tmap_z, const __grid_constant__ CUtensorMap tmap_v) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = (uint8_t *)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // launch order is slot-major (all heads of a chunk slot, then the previous slot): the
-    // CTAs of a wave read whole token rows of q, k, z and v
-    const int32_t xs = prep_slot((int32_t)blockIdx.y, (int32_t)gridDim.y);
-    const int32_t slot = slot0 + xs;
-    const int h = blockIdx.x;
-    int n = 0, L = 0;
-    int64_t t0 = 0;
-    if (!slot_chunk(cu, chunk_off, N, slot, n, t0, L)) return;
-    uint8_t *rec = records + ((size_t)xs * H + h) * REC_BYTES;
-
-    float *TOT = reinterpret_cast<float *>(sm + P_TOT);
-    float *ER = reinterpret_cast<float *>(sm + P_ER);
-    float *RT = reinterpret_cast<float *>(sm + P_RT);
-    float *KTF = reinterpret_cast<float *>(sm + P_KTF);
-    float *BETA = reinterpret_cast<float *>(sm + P_BETA);
     uint64_t *bar = reinterpret_cast<uint64_t *>(sm + P_BAR);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(sm + P_BAR + 16);
     uint64_t *vbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 32);   // the V tile's TMA
     uint64_t *zbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 40);   // the z tile's TMA
     uint64_t *kqbar = reinterpret_cast<uint64_t *>(sm + P_BAR + 48);  // the k and q tiles' TMA
     uint64_t *drain = reinterpret_cast<uint64_t *>(sm + P_BAR + 56);  // products, after a timeout
-
-    // The z, k and q tiles (64 tokens x 128 channels each) arrive by TMA in the 128-byte
-    // swizzled layout, element (r, c) at sw128_offset(r, c, 64), in shared memory that the
-    // element passes overwrite only after reading them.
     if (tid == 0) {
+        // the barriers and the tensor maps, while the chunk's place is looked up
+        tma_prefetch_map(&tmap_z);
+        tma_prefetch_map(&tmap_k);
+        tma_prefetch_map(&tmap_q);
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
         mbar_init(vbar, 1);
@@ -240,6 +225,35 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         mbar_init(kqbar, 1);
         mbar_init(drain, 1);
         fence_mbar_init();
+    }
+    // launch order is slot-major (all heads of a chunk slot, then the previous slot): the
+    // CTAs of a wave read whole token rows of q, k, z and v
+    const int32_t xs = prep_slot((int32_t)blockIdx.y, (int32_t)gridDim.y);
+    const int32_t slot = slot0 + xs;
+    const int h = blockIdx.x;
+    int n = 0, L = 0;
+    int64_t t0 = 0;
+    if (N == 1) {
+        // one sequence, tokens 0 .. T_tot - 1 (cu = [0, T_tot]; other cu values are
+        // reported by the plan kernel): no lookup
+        t0 = (int64_t)slot * C;
+        if (t0 >= T_tot) return;
+        L = (int)min((int64_t)C, T_tot - t0);
+    } else if (!slot_chunk(cu, chunk_off, N, slot, n, t0, L)) {
+        return;
+    }
+    uint8_t *rec = records + ((size_t)xs * H + h) * REC_BYTES;
+
+    float *TOT = reinterpret_cast<float *>(sm + P_TOT);
+    float *ER = reinterpret_cast<float *>(sm + P_ER);
+    float *RT = reinterpret_cast<float *>(sm + P_RT);
+    float *KTF = reinterpret_cast<float *>(sm + P_KTF);
+    float *BETA = reinterpret_cast<float *>(sm + P_BETA);
+
+    // The z, k and q tiles (64 tokens x 128 channels each) arrive by TMA in the 128-byte
+    // swizzled layout, element (r, c) at sw128_offset(r, c, 64), in shared memory that the
+    // element passes overwrite only after reading them.
+    if (tid == 0) {
         mbar_arrive_expect_tx(zbar, 2 * 8192);
         tma_load_3d(sm + P_ZT, &tmap_z, 0, h, (int32_t)t0, zbar);
         tma_load_3d(sm + P_ZT + 8192, &tmap_z, 64, h, (int32_t)t0, zbar);
@@ -1689,8 +1703,8 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         if (rec) rec->mark(sp);
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, sp>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-            (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, recs, st, tm[0], tm[1], tm[2], tm[3]);
+            (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, T_tot,
+            H, (int32_t)s0, recs, st, tm[0], tm[1], tm[2], tm[3]);
         if (rec) rec->mark(sp);
         if (piped) {
             e = cudaEventRecord(P->prep_done[par], sp);
@@ -1758,8 +1772,8 @@ cudaError_t launch_chunk_tc_segmented(const void *q, const void *k, const void *
         dim3 pg((unsigned)H, (unsigned)(s1 - s0));
         prep_kernel<<<pg, PREP_THREADS, P_SMEM, s>>>(
             (const __nv_bfloat16 *)q, (const __nv_bfloat16 *)k, (const __nv_bfloat16 *)v,
-            (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, H,
-            (int32_t)s0, records, st, tm[0], tm[1], tm[2], tm[3]);
+            (const __nv_bfloat16 *)z, (const __nv_bfloat16 *)beta, A_log, cu, chunk_off, N, T_tot,
+            H, (int32_t)s0, records, st, tm[0], tm[1], tm[2], tm[3]);
         const int64_t pairs = std::min<int64_t>(N, s1 - s0) * H;
         const int64_t items1 = pairs * (c32::NBLK + 2 * c32::NBLK * (segs - 1));
         c32::chain_kernel<<<(unsigned)std::min<int64_t>(items1, sm_count), c32::CHAIN_THREADS,

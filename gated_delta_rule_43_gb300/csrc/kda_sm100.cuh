@@ -85,6 +85,10 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+// start fetching a tensor map (a __grid_constant__ kernel parameter) ahead of its first use
+__device__ __forceinline__ void tma_prefetch_map(const void *tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
 // 3-D tiled tensor load through a tensor map (a __grid_constant__ kernel parameter):
 // the box at coordinates (c0 innermost, c1, c2) lands in shared memory as the map's
 // swizzle lays it out; completion counted on `bar`.  c0 * element size must be a

@@ -646,10 +646,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (F) W rows (K-major, rows 0..63 of the record's WQ image) and Ut (fp32) are staged
+    // ---- (F) W rows (K-major, rows 0..63 of the record's WQ image) and Ut (bf16) are staged
     //          in the freed shared memory and leave in three bulk copies.  Rows 0..63 live in
-    //          lane quarters 0 and 1; the warps of those quarters share the 8 tasks (W or Ut)
-    //          x (32-column block), two 16-column TMEM loads in flight per wait.
+    //          lane quarters 0 and 1; the four warps of those quarters take the 4 W tasks
+    //          (32-column blocks), then the 4 Ut tasks, two 16-column TMEM loads in flight per
+    //          wait.  W's copies leave as soon as its staging is complete, while Ut is formed.
     uint8_t *WST = sm + P_WST;   // [2 K halves][64 rows][128 B]
     uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] bf16, pieces swizzled
     if ((warp & 3) < 2) {
@@ -670,6 +671,16 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = i8 < 2 ? lo[8 * i8 + i] : hi[8 * (i8 - 2) + i];
                     *reinterpret_cast<uint4 *>(WST + sw128_offset(rr, 32 * cb + 8 * i8, 64)) = pack8(x);
+                }
+                if (task + PREP_WARPS / 4 >= 4) {
+                    // the last W task of this warp: once all four warps are here, W leaves
+                    fence_proxy_async();
+                    named_bar_sync(1, 128);
+                    if (tid == 0) {
+                        bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
+                        bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
+                        bulk_commit();
+                    }
                 }
             } else {
                 // row rr of column block cb, bf16, pieces swizzled so that the chain
@@ -708,8 +719,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         tc_fence_after();
         tmem_dealloc(tmem, 256);
         if (lane == 0) {
-            bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
-            bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
             bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
             bulk_commit();
             // the CTA may leave once the staging has been read; the writes complete with

@@ -153,6 +153,11 @@ __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool pred) {
     return r != 0;
 }
 
+// Named barrier `id` over `n` threads (a multiple of 32), no predicate
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // executed by one whole warp; the TMEM base address is written to *dst
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {

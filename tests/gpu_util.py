@@ -61,6 +61,24 @@ def oracle_prefill(d, seqs=None, heads=None, o_cmp=None):
                        o_cmp=o_cmp), tok, hsel
 
 
+# The tensor-core path's chunk records, as the library lays them out (74,240 bytes per chunk
+# slot and head, at most 2^30 bytes for one window or a double-buffered pair): tests meant
+# to cross window boundaries assert that their problem does, so that a change of either
+# number cannot quietly make them single-window.
+RECORD_BYTES = 74240
+RECORD_BUDGET = 1 << 30
+
+
+def record_windows(T: int, N: int, H: int) -> int:
+    """Windows of chunk records the tensor-core path runs for T tokens in N sequences."""
+    slots = -(-T // 64) + N
+    w = RECORD_BUDGET // (RECORD_BYTES * H)
+    if slots <= w:
+        return 1
+    half = max(1, w // 2)
+    return -(-slots // half)
+
+
 # the last score_prefill call's worst per-(sequence, head) relative L2 errors (o, state)
 LAST_WORST = {"o": 0.0, "state": 0.0}
 # Sequences shorter than a 16-token tile are left out of the worst per-(sequence, head)

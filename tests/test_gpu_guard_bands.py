@@ -5,12 +5,13 @@ a larger device buffer whose bands before and after it are filled with a sentine
 byte; after the call (and a synchronize) the bands must be unchanged.  The cases
 cover both prefill paths with ragged tails and an empty sequence, the no-alloc
 entry, and dense and indexed decode.  This is the out-of-bounds-write check that
-stands in for a memory sanitizer, which is not available on the GPU pool.
+stands in for a memory sanitizer.
 """
 import pytest
 import torch
 
 from gated_delta_rule_43_gb300 import inputs, kda
+from tests.gpu_util import record_windows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -83,6 +84,7 @@ def test_prefill_writes_stay_in_bounds(dtype, dk, dv):
 
 def test_prefill_many_windows_writes_stay_in_bounds():
     # enough chunk slots x heads that the tensor-core path runs its double-buffered windows
+    assert record_windows(74100, 4, 32) >= 2
     d = inputs.make_prefill([70000, 3, 0, 4097], H=32, dk=128, dv=128, dtype="bf16", seed=62,
                             h0_sigma=0.1, device=DEV)
     _prefill_banded(d)

@@ -3,8 +3,8 @@ import pytest
 import torch
 
 from gated_delta_rule_43_gb300 import inputs, kda
-from tests.gpu_util import (LAST_WORST, TOL, gpu_prefill, rel_l2, score_prefill,
-                            score_prefill_whole, to_f64)
+from tests.gpu_util import (LAST_WORST, TOL, gpu_prefill, record_windows, rel_l2,
+                            score_prefill, score_prefill_whole, to_f64)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -153,6 +153,7 @@ def test_windows_beside_the_chain_long_memory():
     """One sequence long enough for several double-buffered windows of chunk records: the
     prep of window w + 1 runs beside the chain of window w; long-memory gates carry the
     state across every window boundary."""
+    assert record_windows(30000, 1, 32) >= 2
     d = inputs.make_prefill([30000], H=32, dk=128, dv=128, dtype="bf16", seed=31, h0_sigma=0.1,
                             z_shift=-4.0, device=DEV)
     _run_and_score(d, "bf16")
@@ -163,9 +164,10 @@ def test_profiled_entry_pairs_and_stream_order():
     results as kda_chunk_fwd; inputs written on a side stream just before the call, and
     outputs read on it right after, see the call's work in order (the call may run
     kernels on the library's own streams)."""
-    # more than one window of chunk records (1 GiB: 451 chunk slots of 32 heads), so that
-    # the double-buffered schedule with its own streams runs
+    # more than one window of chunk records (451 chunk slots of 32 heads), so that the
+    # double-buffered schedule with its own streams runs
     # (the empty sequence in the middle owns no chunk: its final state is its initial one)
+    assert record_windows(34000, 3, 32) >= 2
     d = inputs.make_prefill([26000, 0, 8000], H=32, dk=128, dv=128, dtype="bf16", seed=77,
                             h0_sigma=0.1, device=DEV)
     T, H, dk = d["q"].shape

@@ -6,13 +6,14 @@ map S_end = M S_start + B is computed in parallel, a scan composes the maps into
 start states and a second pass produces the later segments' outputs.  The
 results must match the fp64 oracle within the bf16 tolerance, for ragged
 sequences, empty ones, initial states, more segments than chunks, and a problem
-large enough to run in two windows.
+large enough to run in several windows.
 """
 import pytest
 import torch
 
 from gated_delta_rule_43_gb300 import inputs, kda
-from tests.gpu_util import LAST_WORST, TOL, gpu_prefill, rel_l2, score_prefill, to_f64
+from tests.gpu_util import (LAST_WORST, TOL, gpu_prefill, record_windows, rel_l2,
+                            score_prefill, to_f64)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -76,10 +77,12 @@ def test_one_segment_is_the_plain_call():
 
 
 def test_two_windows():
-    # 4 heads x 3126 chunk slots of records exceed one 1 GiB window: two windows, the
-    # second starting from the running state the first one's last segment left (long-memory
-    # gates, so that the state carried across the window boundary matters)
-    T = 200_000
+    # 4 heads x 3750 chunk slots of records (74,240 bytes each) exceed one 1 GiB window
+    # (3615 slots): windows of 1807 slots, each after the first starting from the running
+    # state the previous one's last segment left (long-memory gates, so that the state
+    # carried across the window boundaries matters)
+    T = 240_000
+    assert record_windows(T, 1, 4) >= 2
     d = inputs.make_prefill([T], H=4, dk=128, dv=128, dtype="bf16", seed=93, h0_sigma=0.1,
                             z_shift=-6.0, device=DEV)
     o, hT = _seg(d, 4)

@@ -560,12 +560,27 @@ def e2e_bench(args, d, dev, stream, world):
     barrier(world)
     for L in lanes:
         kda.query_status(L["ws"], raise_on_error=True)
-    val, _ = aggregate(T * K, s.elapsed_time(e) / 1e3, world)
+    elapsed = s.elapsed_time(e) / 1e3
+    val, _ = aggregate(T * K, elapsed, world)
+
+    # the host link on its own, for reading the number above: one pinned copy each way
+    def link_gbs(dst, src):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        dst.copy_(src, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        return dst.numel() * dst.element_size() / (a.elapsed_time(b) / 1e3) / 1e9
+    h2d_link = link_gbs(lanes[0]["dev"]["q"], host["q"])
+    d2h_link = link_gbs(lanes[0]["o_h"], lanes[0]["o"])
     return {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K,
+            "h2d_gbs": h2d * K / elapsed / 1e9,
+            "link_h2d_gbs": h2d_link, "link_d2h_gbs": d2h_link,
             "note": "H2D, compute and D2H on three streams with two sets of device buffers: "
                     "the next step's inputs stream in while this step computes and its "
-                    "outputs stream out"}
+                    "outputs stream out; h2d_gbs is the input rate this reached, link_*_gbs "
+                    "one pinned copy of a single tensor each way on its own"}
 
 
 # ----------------------------------------------------------------------------- CPU oracle

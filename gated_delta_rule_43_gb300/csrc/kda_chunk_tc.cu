@@ -779,7 +779,11 @@ namespace c32 {
 constexpr int DVB = 32;          // value columns per CTA
 constexpr int DK_ROWS = DK;      // threads of the scan kernel (one per state row)
 constexpr int NBLK = DV / DVB;
-constexpr int CHAIN_THREADS = 160;   // warps 0-3: rows of S; warp 4: issues [x; P] U
+// warps 0-7: row 32 (w % 4) + lane of S, columns 16 (w / 4) .. + 15 of the block; warp 8
+// issues [x; P] U
+constexpr int CHAIN_THREADS = 288;
+constexpr int ROW_WARPS = 8;
+constexpr int HCOLS = DVB / 2;   // columns a thread holds
 // a record buffer mirrors the record's first 57344 bytes (WQ, KT, P), then this CTA's U
 // block and Gam_C
 constexpr uint32_t B_WQ = 0, B_KT = 32768, B_P = 49152, B_U = 57344, B_G = B_U + UT_BLK;
@@ -802,25 +806,29 @@ __device__ __forceinline__ void chain_load(uint8_t *buf, const uint8_t *rec, int
     bulk_g2s(buf + B_G, rec + REC_G, 512, full);
 }
 
-// 32 fp32 values -> four 16-byte chunks of row r of a 64B-swizzled MN-major image
-__device__ __forceinline__ void store_row_sw64(uint8_t *img, int r, const float (&x)[32]) {
+// 16 fp32 values -> the two 16-byte chunks of row r, columns c0 .. c0 + 15, of a
+// 64B-swizzled MN-major image
+__device__ __forceinline__ void store_half_sw64(uint8_t *img, int r, int c0,
+                                                const float (&x)[HCOLS]) {
 #pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
+    for (int c8 = 0; c8 < 2; ++c8) {
         float y[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) y[i] = x[8 * c8 + i];
-        *reinterpret_cast<uint4 *>(img + sw64_offset(r, 8 * c8, 1)) = pack8(y);
+        *reinterpret_cast<uint4 *>(img + sw64_offset(r, c0 + 8 * c8, 1)) = pack8(y);
     }
 }
 
 // Persistent over work items (sequence, head, 32-column block) of the sequences
 // that own chunks in the slot window [slot0, slot1); each item walks its chunks
-// in order, carrying its block of S in registers (fp32, thread i = row i) and as
+// in order, carrying its block of S in registers (fp32; thread (i, half) holds 16
+// columns of row i) and as
 // the bf16 B operand image.  Per chunk, on the critical path:
 //   D1 = [W; Q*Gam] S  ->  U = Ut - D1[0:64]  ->  D2 = (K*Gam_C/Gam)^T U,
 //   D1 += [x; P] U     ->  S = Diag(Gam_C) S + D2.
 // D1 is double-buffered in TMEM so that the output rows of chunk c (D1[64:128])
-// are stored by warps 2-3 while warps 0-1 form U of chunk c+1.  In the segment-parallel
+// are stored by the warps of lane quarters 2-3 while those of quarters 0-1 form U of
+// chunk c+1.  In the segment-parallel
 // modes (SegArgs) an item is one segment of a sequence's chunks in the window, and a map
 // item walks a 32-column block of [M | B] from [I | 0] (Ut = 0 for the M columns)
 // without storing outputs.
@@ -854,7 +862,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     const uint64_t lim = flt.wait_ns;
     if (tid == 0) {
         for (int x = 0; x < 5; ++x) mbar_init(&bar[x], 1);
-        mbar_init(&bar[5], 2);   // one commit from each issuing warp (0 and 4)
+        mbar_init(&bar[5], 2);   // one commit from each issuing warp (0 and 8)
         mbar_init(&bar[6], 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -868,13 +876,15 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
     tc_fence_after();
     const uint32_t tmem = *tslot;
     const uint32_t D2 = tmem + 64;                     // D1 buffers at columns 0 and 32
-    const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+    const int qr = warp & 3;                           // TMEM lane quarter of this warp
+    const int jc = HCOLS * ((warp >> 2) & 1);          // first column of this thread's half
+    const uint32_t lane_base = ((uint32_t)(32 * qr) << 16) + (uint32_t)jc;
     const uint32_t base = smem_u32(sm);
     const uint32_t id_km = idesc_bf16(128, DVB, false, true);   // A K-major, B MN-major
     const uint32_t id_mm = idesc_bf16(128, DVB, true, true);    // A MN-major, B MN-major
     const uint64_t bd_s = sdesc_sw64(base + C_S, 128 * 64, 512);    // S image, K step 0
     const uint64_t bd_u = sdesc_sw64(base + C_UI, 64 * 64, 512);    // U image 0, K step 0
-    const int i = tid;  // this thread's state row
+    const int i = 32 * qr + lane;  // this thread's state row
     uint32_t gi = 0;    // chunks processed by this CTA (drives buffer and barrier parity)
 
     for (int item = blockIdx.x; item < items && !*abort_flag; item += gridDim.x) {
@@ -909,28 +919,28 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         const int64_t bos = cu[n];
         const int64_t eos = cu[n + 1];
         const int j0 = blk * DVB;
-        float S[DVB];
+        float S[HCOLS];
         const int64_t pairoff = (int64_t)n * H + h;
-        const int64_t soff = (pairoff * DK + i) * DV + j0;
+        const int64_t soff = (pairoff * DK + i) * DV + j0 + jc;
         float *srow = state + soff;
         // the sequence's first chunk starts from h0 (zeros when absent), later windows from
         // the running state, a later segment from its composed start state, a map from
         // the identity (M columns) or zeros (B columns)
         const float *s_in = map ? nullptr
-                          : seg > 0 ? sa.start + ((pairoff * sa.segs + seg) * DK + i) * DV + j0
+                          : seg > 0 ? sa.start + ((pairoff * sa.segs + seg) * DK + i) * DV + j0 + jc
                           : w_begin == cfirst ? (h0 ? h0 + soff : nullptr) : srow;
-        if (warp < 4) {
+        if (warp < ROW_WARPS) {
 #pragma unroll
-            for (int j4 = 0; j4 < DVB / 4; ++j4) {
+            for (int j4 = 0; j4 < HCOLS / 4; ++j4) {
                 const float4 x = s_in ? reinterpret_cast<const float4 *>(s_in)[j4]
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
                 S[4 * j4] = x.x; S[4 * j4 + 1] = x.y; S[4 * j4 + 2] = x.z; S[4 * j4 + 3] = x.w;
             }
             if (mpart) {
 #pragma unroll
-                for (int j = 0; j < DVB; ++j) S[j] = (i == j0 + j) ? 1.f : 0.f;
+                for (int j = 0; j < HCOLS; ++j) S[j] = (i == j0 + jc + j) ? 1.f : 0.f;
             }
-            store_row_sw64(sm + C_S, i, S);
+            store_half_sw64(sm + C_S, i, jc, S);
             fence_proxy_async();
         }
         __syncthreads();
@@ -943,20 +953,21 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         }
 
         // output rows of chunk number `gprev` of this CTA, whose D1 buffer is gprev & 1
-        // (warps 2-3); waits for that chunk's [x; P] U product (barrier m3)
+        // (the warps of lane quarters 2-3); waits for that chunk's [x; P] U product
+        // (barrier m3)
         auto store_o = [&](int32_t cprev, uint32_t gprev) -> bool {
             const uint32_t pb = gprev & 1;
             if (!mbar_wait(&bar[4], gprev & 1, lim)) return false;
             tc_fence_after();
-            const int r = tid - 64;
+            const int r = i - 64;
             const int64_t t = bos + (int64_t)(cprev - cfirst) * C + r;
-            float oacc[32];
-            tmem_ld32(tmem + 32 * pb + lane_base, oacc);
+            float oacc[HCOLS];
+            tmem_ld16(tmem + 32 * pb + lane_base, oacc);
             tmem_ld_wait();
             if (t < eos && !map) {
-                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0);
+                uint4 *dst = reinterpret_cast<uint4 *>(o + (t * H + h) * (int64_t)DV + j0 + jc);
 #pragma unroll
-                for (int i8 = 0; i8 < 4; ++i8) {
+                for (int i8 = 0; i8 < 2; ++i8) {
                     float y[8];
 #pragma unroll
                     for (int x = 0; x < 8; ++x) y[x] = oacc[8 * i8 + x];
@@ -971,10 +982,10 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             const uint32_t b = gi & 1;
             uint8_t *buf = sm + b * BUF_BYTES;
             const uint32_t bufa = base + b * BUF_BYTES;
-            if (warp == 4) {
+            if (warp == ROW_WARPS) {
                 // D1[b] += [x; P] U (outputs only), issued as soon as D2 has been: the
                 // in-order tensor pipe runs it right behind D2, while S is updated and well
-                // before the next D1.  Warp 4 joins no per-chunk barrier.  [x; P] reads the
+                // before the next D1.  This warp joins no per-chunk barrier.  [x; P] reads the
                 // 64 rows in front of P (the tail of KT) as its first half; those rows of D1
                 // hold W S, which the U epilogue has consumed by then.
                 const bool ok4 = __all_sync(0xffffffffu, mbar_wait(&bar[6], gi & 1, lim));
@@ -1012,36 +1023,37 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                 }
                 __syncwarp();
             }
-            if (warp < 2) {
+            if (qr < 2) {
                 // U = Ut - W S  (rows 0..63 live in TMEM lane quarters 0 and 1).  While the
                 // product runs: this thread's row of Ut into registers.  The U image of this
                 // parity was last read two chunks ago, by products the outputs of the
                 // previous chunk waited for.
-                const int r = tid;
-                uint4 ur[4];
+                const int r = i;
+                uint4 ur[2];
 #pragma unroll
-                for (int j = 0; j < 4; ++j)   // the M columns of a map see Ut = 0
+                for (int j = 0; j < 2; ++j)   // the M columns of a map see Ut = 0
                     ur[j] = mpart ? make_uint4(0, 0, 0, 0)
-                                  : *reinterpret_cast<const uint4 *>(buf + B_U + ut_piece(r, j));
+                                  : *reinterpret_cast<const uint4 *>(buf + B_U + ut_piece(r, jc / 8 + j));
                 ok = ok && mbar_wait(&bar[2], gi & 1, lim);
                 tc_fence_after();
                 if (ok) {
-                    float acc[32];
-                    tmem_ld32(tmem + 32 * b + lane_base, acc);
+                    float acc[HCOLS];
+                    tmem_ld16(tmem + 32 * b + lane_base, acc);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < 2; ++j) {
                         float u[8];
                         unpack8(ur[j], u);
 #pragma unroll
                         for (int x = 0; x < 8; ++x) acc[8 * j + x] = u[x] - acc[8 * j + x];
                     }
-                    store_row_sw64(sm + C_UI + b * 4096, r, acc);
+                    store_half_sw64(sm + C_UI + b * 4096, r, jc, acc);
                 }
                 fence_proxy_async();
                 tc_fence_before();
-                // the U image is complete: D2 = (K*Gam_C/Gam)^T U (only warps 0-1 wait here)
-                ok = bar_and(1, 64, ok);
+                // the U image is complete: D2 = (K*Gam_C/Gam)^T U (only the warps of lane
+                // quarters 0-1 wait here)
+                ok = bar_and(1, 128, ok);
                 if (warp == 0 && ok) {
                     tc_fence_after();
                     const uint64_t akt = sdesc_sw128(bufa + B_KT, 64 * 128, 1024);
@@ -1051,7 +1063,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
                             umma_bf16(D2, desc_add(akt, s * 2048), desc_add(bd_u, b * 4096 + s * 1024),
                                       id_mm, s > 0);
                         umma_commit(&bar[3]);
-                        mbar_arrive(&bar[6]);   // warp 4 may queue [x; P] U behind D2
+                        mbar_arrive(&bar[6]);   // the issuing warp may queue [x; P] U behind D2
                     }
                     __syncwarp();
                 }
@@ -1079,18 +1091,18 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
             ok = mbar_wait(&bar[3], gi & 1, lim) && ok;
             tc_fence_after();
             if (ok) {
-                float acc[32];
-                tmem_ld32(D2 + lane_base, acc);
+                float acc[HCOLS];
+                tmem_ld16(D2 + lane_base, acc);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < DVB; ++j) S[j] = gc * S[j] + acc[j];
-                store_row_sw64(sm + C_S, i, S);
+                for (int j = 0; j < HCOLS; ++j) S[j] = gc * S[j] + acc[j];
+                store_half_sw64(sm + C_S, i, jc, S);
             }
             fence_proxy_async();
             tc_fence_before();
-            // warps 0-3: S image complete and this chunk's record reads done; the AND makes
-            // the decision to stop the same for all of them
-            if (!bar_and(2, 128, ok && !*abort_flag)) {
+            // the row warps: S image complete and this chunk's record reads done; the AND
+            // makes the decision to stop the same for all of them
+            if (!bar_and(2, 32 * ROW_WARPS, ok && !*abort_flag)) {
                 if (tid == 0) *abort_flag = 1;
                 aborted = true;
                 break;
@@ -1101,21 +1113,21 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         } else {
             tc_fence_after();
             bool ok_o = true;
-            if (warp >= 2 && warp < 4) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
+            if (qr >= 2 && warp < ROW_WARPS) ok_o = store_o(c_end - 1, gi - 1);   // the item's last chunk
             if (!ok_o) *abort_flag = 1;
             // where the walk's end state goes: the running state, segment 1's start (first
             // pass, segment 0), the map, or nowhere (second pass, all but the last segment:
             // their ends are the next segments' composed starts)
             float *dst = srow;
             if (map)
-                dst = sa.maps + ((pairoff * sa.segs + seg) * DK + i) * (DK + DV) + (mpart ? 0 : DK) + j0;
+                dst = sa.maps + ((pairoff * sa.segs + seg) * DK + i) * (DK + DV) + (mpart ? 0 : DK) + j0 + jc;
             else if (sa.mode == 1 && s_eff > 1)
-                dst = sa.start + ((pairoff * sa.segs + 1) * DK + i) * DV + j0;
+                dst = sa.start + ((pairoff * sa.segs + 1) * DK + i) * DV + j0 + jc;
             else if (sa.mode == 2 && seg != s_eff - 1)
                 dst = nullptr;
-            if (warp < 4 && dst) {
+            if (warp < ROW_WARPS && dst) {
 #pragma unroll
-                for (int j4 = 0; j4 < DVB / 4; ++j4)
+                for (int j4 = 0; j4 < HCOLS / 4; ++j4)
                     reinterpret_cast<float4 *>(dst)[j4] =
                         make_float4(S[4 * j4], S[4 * j4 + 1], S[4 * j4 + 2], S[4 * j4 + 3]);
             }
@@ -1128,7 +1140,7 @@ chain_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__ chunk_o
         // an expired wait: the products both issuing warps committed and the record loads
         // still in flight finish (each wait bounded again) before the tensor memory is
         // released and the CTA leaves
-        if (warp == 0 || warp == 4) {
+        if (warp == 0 || warp == ROW_WARPS) {
             tc_fence_after();
             if (elect_one()) umma_commit(&bar[5]);
             __syncwarp();

@@ -192,10 +192,9 @@ __device__ __forceinline__ bool slot_chunk(const int32_t *cu, const int32_t *chu
 // the chain kernel reads first, are the most recently written (still in L2).
 __device__ __forceinline__ int32_t prep_slot(int32_t y, int32_t nslots) { return nslots - 1 - y; }
 
-// One CTA per (chunk slot, head).  Work split for the row-wise element passes: lane l of
-// warp w takes the 8-channel chunk ch = 2w + (l >> 4) of rows 16u + (l & 15), one in each
-// 16-token tile u = 0..3.  The in-tile cumulative sums run down the columns of a
-// shared-memory scratch, one (tile, channel) per thread.
+// One CTA per (chunk slot, head).  The gate and the in-tile cumulative sums take one
+// (tile, channel) column per thread; the row-wise element passes that follow give each
+// thread 8 channels of one row in each 16-token tile.
 __global__ void __launch_bounds__(PREP_THREADS, 2)
 prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict__ k,
             const __nv_bfloat16 *__restrict__ v, const __nv_bfloat16 *__restrict__ z,
@@ -277,47 +276,42 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (tid < C) BETA[tid] = beta_v;
     __syncthreads();                           // the barriers' initialisation is visible
     bool ok = mbar_wait(zbar, 0);
-    uint4 zraw[NU];
-#pragma unroll
-    for (int u = 0; u < NU; ++u)
-        zraw[u] = *reinterpret_cast<const uint4 *>(sm + P_ZT + sw128_offset(16 * u + rl, c, 64));
-
-    // ---- (A) gate into the fp32 G scratch (row-wise, 16-byte stores), then the in-tile
-    //          inclusive cumsums down the columns: thread (tile, channel) walks its 16 rows,
-    //          leaves G in place, records the tile sum and checks the range.  Every g lies in
-    //          [g_min, 0] (NaN aside), so a tile's cumulative decay falls monotonically from 0
-    //          and stays in [-80, 0] iff its last value does; a NaN reaches the last value
-    //          too.  Only a tile whose last value fails is searched for its first bad row.
+    // ---- (A) gate and in-tile inclusive cumsums, fused: thread (tile ta, position p) reads
+    //          its column of z from the swizzled tile (a warp's 32 positions share one
+    //          128-byte line of a row), forms each g, accumulates G down the tile's 16 rows
+    //          in a register and writes it into the fp32 G scratch; the tile sum goes to
+    //          TOT.  Every g lies in [g_min, 0] (NaN aside), so a tile's cumulative decay
+    //          falls monotonically from 0 and stays in [-80, 0] iff its last value does; a
+    //          NaN reaches the last value too.  Only a tile whose last value fails is
+    //          searched for its first bad row.
     float *GS = reinterpret_cast<float *>(sm + P_G);
+    {
+        const int p = tid & (DK - 1);
+        const int ch = pos_chan(p);
 #pragma unroll
-    for (int u = 0; u < NU; ++u) {   // g = -5 / (1 + 2^(-e^A log2(e) z)); NaN stays NaN
-        const int r = 16 * u + rl;
-        float zz[8];
-        unpack8(zraw[u], zz);
+        for (int half = 0; half < 2; ++half) {
+            const int ta = (tid >> 7) + 2 * half;
+            float zz[16];
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            zz[i] = r < L ? kGMin * rcp_approx(1.0f + ex2_approx(nl2e * zz[i])) : 0.f;
-        float *dst = GS + r * GLD + chan_pos(c);
-        *reinterpret_cast<float4 *>(dst) = make_float4(zz[0], zz[1], zz[2], zz[3]);
-        *reinterpret_cast<float4 *>(dst + 32) = make_float4(zz[4], zz[5], zz[6], zz[7]);
-    }
-    __syncthreads();
+            for (int i = 0; i < 16; ++i) {
+                const uint32_t bits = *reinterpret_cast<const uint16_t *>(
+                    sm + P_ZT + sw128_offset(16 * ta + i, ch, 64));
+                zz[i] = __uint_as_float(bits << 16);
+            }
+            float run = 0.f;
 #pragma unroll
-    for (int e = tid; e < 4 * DK; e += PREP_THREADS) {   // (tile, position) pairs
-        const int ta = e >> 7, c = e & (DK - 1);
-        float *col = GS + (16 * ta) * GLD + c;
-        float run = 0.f;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            run += col[i * GLD];
-            col[i * GLD] = run;
-        }
-        TOT[ta * DK + c] = run;
-        if (!decay_ok(run)) {
-            int bad_row = -1;
-            for (int i = 0; i < 16 && bad_row < 0; ++i)
-                if (16 * ta + i < L && !decay_ok(col[i * GLD])) bad_row = 16 * ta + i;
-            if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
+            for (int i = 0; i < 16; ++i) {   // g = -5 / (1 + 2^(-e^A log2(e) z)); NaN stays NaN
+                const int r = 16 * ta + i;
+                run += r < L ? kGMin * rcp_approx(1.0f + ex2_approx(nl2e * zz[i])) : 0.f;
+                GS[r * GLD + p] = run;
+            }
+            TOT[ta * DK + p] = run;
+            if (!decay_ok(run)) {
+                int bad_row = -1;
+                for (int i = 0; i < 16 && bad_row < 0; ++i)
+                    if (16 * ta + i < L && !decay_ok(GS[(16 * ta + i) * GLD + p])) bad_row = 16 * ta + i;
+                if (bad_row >= 0) report(st, KDA_ERR_DECAY_RANGE, (t0 + bad_row) * H + h, 5);
+            }
         }
     }
     __syncthreads();

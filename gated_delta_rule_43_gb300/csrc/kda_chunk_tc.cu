@@ -94,7 +94,6 @@ constexpr uint32_t P_ZT = 47104;        // (until pass A) z tile, TMA, [2][64][1
 constexpr uint32_t P_KT = 63488;        // (until the table pass) k tile, likewise
 constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewise
 constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], over the dead tables
-constexpr uint32_t P_QST = 87040;       // (pass B) Q*Gam staging [2][64][128 B], before T diag(b)
 constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
 constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, bf16 [4][64][32]
 constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
@@ -107,7 +106,7 @@ static_assert(P_G + 64 * GLD * 4 <= P_TB, "G scratch overlaps the T diag(b) imag
 static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024 == 0 &&
                   P_KT % 1024 == 0 && P_QT % 1024 == 0, "raw tiles");
 static_assert(P_WST + 16384 <= P_AS && P_UST + 16384 <= P_TB &&
-                  P_PST + 8192 <= P_BETA && P_QST + 16384 <= P_END,
+                  P_PST + 8192 <= P_BETA,
               "solve / epilogue staging overlaps live data");
 static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
@@ -382,7 +381,7 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const uint32_t row = 32 * a + rl;
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row, c, 128)) = pack8(kr);
         *reinterpret_cast<uint4 *>(sm + P_KRQR + sw128_offset(row + 16, c, 128)) = pack8(qr);
-        *reinterpret_cast<uint4 *>(sm + P_QST + sw128_offset(r, c, 64)) = pack8(qg);
+        *reinterpret_cast<uint4 *>(rec + REC_WQ + sw128_offset(64 + r, c, 128)) = pack8(qg);
         *reinterpret_cast<uint4 *>(rec + REC_KT + sw128_offset(r, c, 64)) = pack8(kt);
         // image a2 >= a holds row r scaled by exp(ref_a2 - G_r) = kf * exp(ref_a2 - ref_a);
         // image a2 occupies rows 8 a2 (a2 + 1) .. of the stacked [160][128] B operand
@@ -416,12 +415,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             umma_commit(&bar[0]);
         }
         __syncwarp();
-        if (lane == 0) {
-            // Q*Gam (staged in pass B) -> rows 64..127 of the record's WQ image, both K halves
-            bulk_s2g(rec + REC_WQ + 8192, sm + P_QST, 8192);
-            bulk_s2g(rec + REC_WQ + 16384 + 8192, sm + P_QST + 8192, 8192);
-            bulk_commit();
-        }
     }
     ok = mbar_wait(&bar[0], 0) && ok;
     tc_fence_after();
@@ -495,10 +488,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
     //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
-    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E) shares its region
-    // with the Q*Gam staging, whose bulk copy is given until the N^3 step to finish; it is
-    // written there: zero blocks above the diagonal in the N^3 step, the other blocks in
-    // the last step of the solve.
+    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E): zero blocks
+    // above the diagonal in the N^3 step, the other blocks in the last step of the solve.
     uint8_t *TBI = sm + P_TB;
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
     auto pair_a = [](int pr) { return pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3); };
@@ -554,7 +545,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         *reinterpret_cast<float4 *>(XS + q * 16 * XLD + i * XLD + 4 * jq) = x;
     }
-    if (tid == 0) bulk_wait_read_all();   // the Q*Gam staging (the T diag(b) region) is free
     __syncthreads();
     if (tid < 64) {  // N^3_30 = N32 N^2_20
         const int i = tid >> 2, jq = tid & 3;

@@ -96,8 +96,11 @@ constexpr uint32_t P_QT = 79872;        // (until the table pass) q tile, likewi
 constexpr uint32_t P_PST = 1024;        // (A/P epilogue) P staging, K-major [64][64], over the dead tables
 constexpr uint32_t P_WST = 13312;       // (epilogue) W staging, K-major [2][64][128 B]
 constexpr uint32_t P_UST = 46080;       // (epilogue) Ut staging, bf16 [4][64][32]
-constexpr uint32_t P_TB = 87040;        // K-major [64][64] T diag(b); the M=128 operand's rows
-constexpr uint32_t P_END = 103424;      //   64..127 read the next 8 KB (ignored rows)
+// The A operand of step E, [T diag(b), 0; 0, T diag(b)] (K-major, 128 rows, K = 2C), in two
+// 64-column halves: half 0 over the dead fp32 A, half 1 at the end
+constexpr uint32_t P_A0 = P_AS;         //   half 0: T diag(b) in rows 0..63, zeros below
+constexpr uint32_t P_TB = 87040;        //   half 1: zeros in rows 0..63, T diag(b) below
+constexpr uint32_t P_END = 103424;
 constexpr uint32_t P_SMEM = P_END + 1024;
 static_assert(P_KC + 4096 + 8192 + 12288 + 16384 <= P_TB, "column-scaled K images overflow");
 static_assert(P_KGV + 32768 <= P_AS && P_AS + 64 * LDA * 4 <= P_TS, "prep smem reuse overlaps");
@@ -108,7 +111,8 @@ static_assert(P_ZT >= P_G + 64 * GLD * 4 && P_QT + 16384 <= P_END && P_ZT % 1024
 static_assert(P_WST + 16384 <= P_AS && P_UST + 16384 <= P_TB &&
                   P_PST + 8192 <= P_BETA,
               "solve / epilogue staging overlaps live data");
-static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0, "image alignment");
+static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0 && P_A0 % 1024 == 0 &&
+                  P_A0 + 16384 <= P_TS, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
 __device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
@@ -416,6 +420,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         }
         __syncwarp();
     }
+    // while the products run: the zero rows 0..63 of step E's operand half 1 (the q tile
+    // that held this region has been read)
+#pragma unroll
+    for (int e = tid; e < 512; e += PREP_THREADS)
+        *reinterpret_cast<uint4 *>(sm + P_TB + 16 * e) = make_uint4(0, 0, 0, 0);
     ok = mbar_wait(&bar[0], 0) && ok;
     tc_fence_after();
     // ---- (C) MN-major [K*Gam | V] image in the freed [Kr; Qr] region: the V half arrives
@@ -488,9 +497,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     // ---- (D) T = (I + A)^-1 in fp32 over 16x16 blocks.  With D = blockdiag(I + A_aa) and
     //          N = D^-1 (A - blockdiag(A_aa)) (block strictly lower, so N^4 = 0):
     //          T = (I + N)^-1 D^-1 = (I - N + N^2 - N^3) D^-1.
-    // The T diag(b) image (K-major [64][64] bf16, the A operand of step E): zero blocks
-    // above the diagonal in the N^3 step, the other blocks in the last step of the solve.
-    uint8_t *TBI = sm + P_TB;
+    // T diag(b) (K-major [64][64] bf16) goes into both diagonal blocks of step E's operand:
+    // zero blocks above the diagonal in the N^3 step, the other blocks in the last step of
+    // the solve; the zero block under half 0's copy in the N^2 step.
+    uint8_t *TBI0 = sm + P_A0;
+    uint8_t *TBI1 = sm + P_TB + 8192;   // rows 64.. of half 1 share the swizzle of rows 0..
     // off-diagonal block pairs (a, b), a > b, numbered (1,0) (2,1) (3,2) (2,0) (3,1) (3,0).
     auto pair_a = [](int pr) { return pr < 3 ? pr + 1 : (pr == 3 ? 2 : 3); };
     auto pair_b = [](int pr) { return pr < 3 ? pr : (pr == 4 ? 1 : 0); };
@@ -544,6 +555,11 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             acc16(x, nrow(2, i), ncol(3, jq), LDA);
         }
         *reinterpret_cast<float4 *>(XS + q * 16 * XLD + i * XLD + 4 * jq) = x;
+    } else {
+        // rows 64..127 of half 0 (over the fp32 A, which the diagonal step has consumed)
+#pragma unroll
+        for (int e = tid - 192; e < 512; e += PREP_THREADS - 192)
+            *reinterpret_cast<uint4 *>(sm + P_A0 + 8192 + 16 * e) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     if (tid < 64) {  // N^3_30 = N32 N^2_20
@@ -556,8 +572,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
         const int e = tid - 64, ub = e >> 5, rc = e & 31;
         const int ua = ub < 3 ? 0 : (ub < 5 ? 1 : 2);
         const int uc = ub < 3 ? ub + 1 : (ub < 5 ? ub - 1 : 3);
-        *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64)) =
-            make_uint4(0, 0, 0, 0);
+        const uint32_t off = sw128_offset(16 * ua + (rc >> 1), 16 * uc + 8 * (rc & 1), 64);
+        *reinterpret_cast<uint4 *>(TBI0 + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4 *>(TBI1 + off) = make_uint4(0, 0, 0, 0);
     }
     __syncthreads();
     // T_ab = M_ab T_bb with M = -N + N^2 - N^3 (blockwise), scaled by b and written to the image
@@ -586,7 +603,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             uint2 pk;
             *reinterpret_cast<__nv_bfloat162 *>(&pk.x) = __floats2bfloat162_rn(x.x * bb.x, x.y * bb.y);
             *reinterpret_cast<__nv_bfloat162 *>(&pk.y) = __floats2bfloat162_rn(x.z * bb.z, x.w * bb.w);
-            *reinterpret_cast<uint2 *>(TBI + sw128_offset(16 * a2 + i, 16 * b + 4 * jq, 64)) = pk;
+            const uint32_t off = sw128_offset(16 * a2 + i, 16 * b + 4 * jq, 64);
+            *reinterpret_cast<uint2 *>(TBI0 + off) = pk;
+            *reinterpret_cast<uint2 *>(TBI1 + off) = pk;
         } else if (task < 384 + 128) {
             // diagonal blocks: (block tb, row i, 8-column half) -> one 16-byte chunk
             const int e = task - 384, tb = e >> 5, i = (e >> 1) & 15, hf = e & 1;
@@ -595,7 +614,9 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             ld8(BETA + 16 * tb + 8 * hf, bt);
 #pragma unroll
             for (int c = 0; c < 8; ++c) x[c] = tt[c] * bt[c];
-            *reinterpret_cast<uint4 *>(TBI + sw128_offset(16 * tb + i, 16 * tb + 8 * hf, 64)) = pack8(x);
+            const uint32_t off = sw128_offset(16 * tb + i, 16 * tb + 8 * hf, 64);
+            *reinterpret_cast<uint4 *>(TBI0 + off) = pack8(x);
+            *reinterpret_cast<uint4 *>(TBI1 + off) = pack8(x);
         }
     }
     if (L < C) {
@@ -612,17 +633,21 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     tc_fence_before();
     __syncthreads();
 
-    // ---- (E) [W | Ut] = T diag(b) [K*Gam | V]  (M = 128: rows 64.. are ignored)
+    // ---- (E) [W; Ut] = [T diag(b), 0; 0, T diag(b)] [K*Gam; V]  (M = 128, N = 128, K = 2C):
+    //          W in TMEM lanes 0..63, Ut in lanes 64..127, so that all eight warps share
+    //          the epilogue.  K steps 0..3 read K*Gam and operand half 0, steps 4..7 V and half 1.
     if (warp == 0) {
         ok = mbar_wait(vbar, 0) && ok;
         tc_fence_after();
-        const uint32_t idesc = idesc_bf16(128, 256, false, true);
-        const uint64_t ad = sdesc_sw128(base + P_TB, 16, 1024);
+        const uint32_t idesc = idesc_bf16(128, DK, false, true);
+        const uint64_t a0 = sdesc_sw128(base + P_A0, 16, 1024);
+        const uint64_t a1 = sdesc_sw128(base + P_TB, 16, 1024);
         const uint64_t bd = sdesc_sw128(base + P_KGV, 64 * 128, 1024);
         if (elect_one()) {
 #pragma unroll
-            for (int s = 0; s < C / 16; ++s)
-                umma_bf16(tmem, desc_add(ad, s * 32), desc_add(bd, s * 2048), idesc, s > 0);
+            for (int s = 0; s < 2 * C / 16; ++s)
+                umma_bf16(tmem, desc_add(s < 4 ? a0 : a1, (s & 3) * 32),
+                          desc_add(bd, (s >> 2) * 16384 + (s & 3) * 2048), idesc, s > 0);
             umma_commit(&bar[1]);
         }
         __syncwarp();
@@ -630,23 +655,24 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     ok = mbar_wait(&bar[1], 0) && ok;
     tc_fence_after();
 
-    // ---- (F) W rows (K-major, rows 0..63 of the record's WQ image) and Ut (bf16) are staged
-    //          in the freed shared memory and leave in three bulk copies.  Rows 0..63 live in
-    //          lane quarters 0 and 1; the four warps of those quarters take the 4 W tasks
-    //          (32-column blocks), then the 4 Ut tasks, two 16-column TMEM loads in flight per
-    //          wait.  W's copies leave as soon as its staging is complete, while Ut is formed.
+    // ---- (F) W (lanes 0..63; K-major, rows 0..63 of the record's WQ image) and Ut (lanes
+    //          64..127, bf16) are staged in the freed shared memory and leave in three bulk
+    //          copies.  Warp w takes lane quarter w & 3 and the 32-column blocks 2 (w >> 2) and
+    //          2 (w >> 2) + 1, two 16-column TMEM loads in flight per wait; W's copies leave
+    //          once its four warps have staged it, Ut's once its four have.
     uint8_t *WST = sm + P_WST;   // [2 K halves][64 rows][128 B]
     uint8_t *UST = sm + P_UST;   // [4 column blocks][64 rows][32] bf16, pieces swizzled
-    if ((warp & 3) < 2) {
+    {
         const int quarter = warp & 3;
-        const int rr = 32 * quarter + lane;
+        const bool isW = quarter < 2;
+        const int rr = 32 * (quarter & 1) + lane;
         const uint32_t src = tmem + ((uint32_t)(32 * quarter) << 16);
-        for (int task = warp >> 2; task < 8; task += PREP_WARPS / 4) {
-            const bool isW = task < 4;
-            const int cb = task & 3;
+#pragma unroll
+        for (int t2 = 0; t2 < 2; ++t2) {
+            const int cb = 2 * (warp >> 2) + t2;
             float lo[16], hi[16];
-            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb, lo);
-            tmem_ld16(src + (isW ? 0 : 128) + 32 * cb + 16, hi);
+            tmem_ld16(src + 32 * cb, lo);
+            tmem_ld16(src + 32 * cb + 16, hi);
             tmem_ld_wait();
             if (isW) {
 #pragma unroll
@@ -655,16 +681,6 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
 #pragma unroll
                     for (int i = 0; i < 8; ++i) x[i] = i8 < 2 ? lo[8 * i8 + i] : hi[8 * (i8 - 2) + i];
                     *reinterpret_cast<uint4 *>(WST + sw128_offset(rr, 32 * cb + 8 * i8, 64)) = pack8(x);
-                }
-                if (task + PREP_WARPS / 4 >= 4) {
-                    // the last W task of this warp: once all four warps are here, W leaves
-                    fence_proxy_async();
-                    named_bar_sync(1, 128);
-                    if (tid == 0) {
-                        bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
-                        bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
-                        bulk_commit();
-                    }
                 }
             } else {
                 // row rr of column block cb, bf16, pieces swizzled so that the chain
@@ -678,6 +694,17 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
                     *reinterpret_cast<uint4 *>(dst + ut_piece(rr, j)) = pack8(x);
                 }
             }
+        }
+        fence_proxy_async();
+        if (isW) named_bar_sync(1, 128);   // constant barrier ids
+        else named_bar_sync(2, 128);
+        if (tid == 0) {
+            bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
+            bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1
+            bulk_commit();
+        } else if (tid == 64) {
+            bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
+            bulk_commit();
         }
     }
     fence_proxy_async();
@@ -702,14 +729,10 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
     if (warp == 0) {
         tc_fence_after();
         tmem_dealloc(tmem, 256);
-        if (lane == 0) {
-            bulk_s2g(rec + REC_U, UST, REC_G - REC_U);         // Ut
-            bulk_commit();
-            // the CTA may leave once the staging has been read; the writes complete with
-            // the kernel, before anything ordered after it reads the records
-            bulk_wait_read_all();
-        }
     }
+    // the CTA may leave once its staging has been read (threads 0 and 64 issued the copies);
+    // the writes complete with the kernel, before anything ordered after it reads the records
+    if (tid == 0 || tid == 64) bulk_wait_read_all();
 }
 
 // ---------------------------------------------------------------- chain kernels

@@ -696,8 +696,8 @@ prep_kernel(const __nv_bfloat16 *__restrict__ q, const __nv_bfloat16 *__restrict
             }
         }
         fence_proxy_async();
-        if (isW) named_bar_sync(1, 128);   // constant barrier ids
-        else named_bar_sync(2, 128);
+        if (isW) named_bar_sync(1, 128);   // the four W warps
+        else named_bar_sync(2, 128);       // the four Ut warps
         if (tid == 0) {
             bulk_s2g(rec + REC_WQ, WST, 8192);                 // W, K half 0
             bulk_s2g(rec + REC_WQ + 16384, WST + 8192, 8192);  // W, K half 1

@@ -115,9 +115,6 @@ static_assert(P_KRQR % 1024 == 0 && P_KC % 1024 == 0 && P_TB % 1024 == 0 && P_A0
                   P_A0 + 16384 <= P_TS, "image alignment");
 static_assert(P_TB + 16384 == P_END && 2 * (P_SMEM + 1024) <= 233472, "two CTAs per SM");
 
-__device__ __forceinline__ void st_bf16(uint8_t *base, uint32_t off, float x) {
-    *reinterpret_cast<__nv_bfloat16 *>(base + off) = __float2bfloat16_rn(x);
-}
 __device__ __forceinline__ uint4 pack8(const float (&x)[8]) {
     uint4 r;
     __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&r);

@@ -1712,7 +1712,6 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
     }
     const size_t buf_bytes = (size_t)window * H * REC_BYTES;
     int64_t w = 0;
-    bool prev_narrow = false;   // the previous window's chain is the 32-column kernel
     for (int64_t s0 = 0; s0 < slots; s0 += window, ++w) {
         const int64_t s1 = std::min(slots, s0 + window);
         const int par = (int)(w & 1);
@@ -1720,12 +1719,9 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         cudaStream_t sp = piped ? P->prep[par] : s;
         cudaStream_t sc = piped ? P->chain : s;
         // prep of window w; with two buffers, after the chain of window w - 2 has read
-        // this buffer.  Behind a 32-column chain (a latency-bound walk on whole SMs, the
-        // step's critical path) also after the prep of window w - 1, so that the chain of
-        // window w - 1 takes the SMs its prep's last CTAs free before this prep does
+        // this buffer
         if (piped && w >= 2) {
             e = cudaStreamWaitEvent(sp, P->chain_done[par], 0);
-            if (e == cudaSuccess && prev_narrow) e = cudaStreamWaitEvent(sp, P->prep_done[par ^ 1], 0);
             if (e != cudaSuccess) return e;
         }
         dim3 pg((unsigned)H, (unsigned)(s1 - s0));   // slot-major; a window holds < 65536 slots
@@ -1748,8 +1744,7 @@ cudaError_t launch_chunk_tc(const void *q, const void *k, const void *v, const v
         const int64_t seqs = std::min<int64_t>(N, s1 - s0);
         const int64_t items32 = seqs * H * c32::NBLK;
         if (rec) rec->mark(sc);
-        prev_narrow = items32 <= (piped ? (int64_t)sm_count / 2 : 2 * (int64_t)sm_count);
-        if (prev_narrow) {
+        if (items32 <= (piped ? (int64_t)sm_count / 2 : 2 * (int64_t)sm_count)) {
             const int64_t grid = std::min<int64_t>(seqs * H * c32::NBLK, sm_count);
             c32::chain_kernel<<<(unsigned)grid, c32::CHAIN_THREADS, c32::C_SMEM, sc>>>(
                 cu, chunk_off, N, H, (int32_t)s0, (int32_t)s1, recs, h0, S_run,

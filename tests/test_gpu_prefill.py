@@ -149,6 +149,19 @@ def test_both_chain_shapes(lens):
 
 
 @pytest.mark.timeout(900)
+def test_windows_one_head_chain_slower_than_prep():
+    """One head, about a million tokens: three windows, each window's prep far shorter than
+    the previous window's chain, so that a window's chain must wait for the previous chain
+    (its start state) as well as for its own prep, and the next prep must not overwrite the
+    records of a chain still running."""
+    T = 1_000_000
+    assert record_windows(T, 1, 1) >= 3
+    d = inputs.make_prefill([T], H=1, dk=128, dv=128, dtype="bf16", seed=41, h0_sigma=0.1,
+                            z_shift=-4.0, device=DEV)
+    _run_and_score(d, "bf16")
+
+
+@pytest.mark.timeout(900)
 def test_windows_beside_the_chain_long_memory():
     """One sequence long enough for several double-buffered windows of chunk records: the
     prep of window w + 1 runs beside the chain of window w; long-memory gates carry the

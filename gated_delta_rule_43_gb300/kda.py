@@ -101,6 +101,48 @@ def _check_cuda(*ts):
                 raise ValueError("tensors must be contiguous")
 
 
+def _expect(name, t, shape, dtype=None):
+    """t (when given) has exactly `shape` (and `dtype`): the C ABI takes raw pointers and
+    sizes, so a tensor smaller than the sizes say would be read or written past its end."""
+    if t is None:
+        return
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} has dtype {t.dtype}, expected {dtype}")
+
+
+def _check_step_inputs(q, k, v, z, beta, A_log, lead):
+    """q, k, z [*lead, H, dk], v [*lead, H, dv], beta [*lead, H], one dtype (fp32 or bf16);
+    A_log [H] fp32.  Returns (H, dk, dv)."""
+    if q.dim() != len(lead) + 2 or v.dim() != len(lead) + 2:
+        raise ValueError(f"q and v must be [{', '.join(map(str, lead))}, H, D]")
+    H, dk = q.shape[-2:]
+    dv = v.shape[-1]
+    if q.dtype not in _DT:
+        raise TypeError(f"q has dtype {q.dtype}; fp32 and bf16 are supported")
+    _expect("k", k, (*lead, H, dk), q.dtype)
+    _expect("z", z, (*lead, H, dk), q.dtype)
+    _expect("v", v, (*lead, H, dv), q.dtype)
+    _expect("beta", beta, (*lead, H), q.dtype)
+    _expect("A_log", A_log, (H,), torch.float32)
+    return H, dk, dv
+
+
+def _check_prefill(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state):
+    if q.dim() != 3:
+        raise ValueError("q must be [T, H, dk]")
+    T = q.shape[0]
+    H, dk, dv = _check_step_inputs(q, k, v, z, beta, A_log, (T,))
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be a 1-D int32 tensor [N + 1]")
+    N = cu_seqlens.numel() - 1
+    _expect("initial_state", initial_state, (N, H, dk, dv), torch.float32)
+    _expect("final_state", final_state, (N, H, dk, dv), torch.float32)
+    _expect("o", o, (T, H, dv), q.dtype)
+    return T, N, H, dk, dv
+
+
 def chunk_fwd_workspace_size(total_tokens: int, num_seqs: int, H: int, dk: int, dv: int,
                              dtype: torch.dtype) -> int:
     return int(load().kda_chunk_fwd_workspace_size(total_tokens, num_seqs, H, dk, dv,
@@ -125,13 +167,10 @@ def chunk_fwd(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None, *,
     raises KdaError.
     """
     lib = load()
+    T, N, H, dk, dv = _check_prefill(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o,
+                                     final_state)
     _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = cu_seqlens.numel() - 1
     dt = _DT[q.dtype]
-    if A_log.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
-        raise TypeError("A_log must be fp32 and cu_seqlens int32")
     if o is None:
         o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
@@ -156,13 +195,10 @@ def chunk_fwd_segmented(q, k, v, z, beta, A_log, cu_seqlens, initial_state=None,
     """Segment-parallel prefill (kda_chunk_fwd_segmented): chunk_fwd's arguments and
     results, each sequence's chunks of a window cut into up to ``segments`` segments."""
     lib = load()
+    T, N, H, dk, dv = _check_prefill(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o,
+                                     final_state)
     _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = cu_seqlens.numel() - 1
     dt = _DT[q.dtype]
-    if A_log.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
-        raise TypeError("A_log must be fp32 and cu_seqlens int32")
     if o is None:
         o = torch.empty(T, H, dv, dtype=q.dtype, device=q.device)
     if final_state is None and output_final_state:
@@ -191,10 +227,9 @@ def chunk_fwd_profiled(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, fi
     both recorded on the stream that kernel was launched on.
     """
     lib = load()
+    T, N, H, dk, dv = _check_prefill(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o,
+                                     final_state)
     _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, workspace)
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = cu_seqlens.numel() - 1
     for e in events:
         if not e.cuda_event:  # torch creates the CUDA event on its first record
             e.record(stream if stream is not None else torch.cuda.current_stream())
@@ -219,10 +254,11 @@ def chunk_fwd_noalloc(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, fin
     shared scratch must not overlap between calls (serialise them).
     """
     lib = load()
+    T, N, H, dk, dv = _check_prefill(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o,
+                                     final_state)
     _check_cuda(q, k, v, z, beta, A_log, cu_seqlens, initial_state, o, final_state, status_out)
-    T, H, dk = q.shape
-    dv = v.shape[-1]
-    N = cu_seqlens.numel() - 1
+    if status_out is not None and status_out.numel() * status_out.element_size() < 16:
+        raise ValueError("status_out must hold at least 16 bytes")
     rc = lib.kda_chunk_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(beta), _ptr(A_log),
                                    _ptr(cu_seqlens), N, T, H, dk, dv, _DT[q.dtype],
                                    _ptr(initial_state), _ptr(final_state), _ptr(o),
@@ -239,11 +275,13 @@ def decode_step(q, k, v, z, beta, A_log, state, *, o=None, workspace=None, strea
     Returns o [N, H, dv].
     """
     lib = load()
+    if q.dim() != 3:
+        raise ValueError("q must be [N, H, dk]")
+    N = q.shape[0]
+    H, dk, dv = _check_step_inputs(q, k, v, z, beta, A_log, (N,))
+    _expect("state", state, (N, H, dk, dv), torch.float32)
+    _expect("o", o, (N, H, dv), q.dtype)
     _check_cuda(q, k, v, z, beta, A_log, state, o, workspace)
-    N, H, dk = q.shape
-    dv = v.shape[-1]
-    if state.dtype != torch.float32:
-        raise TypeError("state must be fp32")
     if o is None:
         o = torch.empty(N, H, dv, dtype=q.dtype, device=q.device)
     if workspace is None:
@@ -264,11 +302,14 @@ def decode_step_indexed(q, k, v, z, beta, A_log, state_pool, state_idx, *, o=Non
     state_idx [N] int32 (distinct values in [0, P)).  Returns o [N, H, dv].
     """
     lib = load()
+    if q.dim() != 3 or state_pool.dim() != 4:
+        raise ValueError("q must be [N, H, dk] and state_pool [P, H, dk, dv]")
+    N = q.shape[0]
+    H, dk, dv = _check_step_inputs(q, k, v, z, beta, A_log, (N,))
+    _expect("state_pool", state_pool, (state_pool.shape[0], H, dk, dv), torch.float32)
+    _expect("state_idx", state_idx, (N,), torch.int32)
+    _expect("o", o, (N, H, dv), q.dtype)
     _check_cuda(q, k, v, z, beta, A_log, state_pool, state_idx, o, workspace)
-    N, H, dk = q.shape
-    dv = v.shape[-1]
-    if state_pool.dtype != torch.float32 or state_idx.dtype != torch.int32:
-        raise TypeError("state_pool must be fp32 and state_idx int32")
     if o is None:
         o = torch.empty(N, H, dv, dtype=q.dtype, device=q.device)
     if workspace is None:
@@ -291,8 +332,13 @@ def gate_cumsum(z, A_log, cu_seqlens, chunk: int = 64, *, softplus: bool = False
     softplus=True evaluates the unbounded -Softplus baseline instead of the
     lower-bounded gate (same 16-token range check)."""
     lib = load()
-    _check_cuda(z, A_log, cu_seqlens, workspace)
+    if z.dim() != 3 or z.dtype not in _DT:
+        raise ValueError("z must be [T, H, dk], fp32 or bf16")
     T, H, dk = z.shape
+    _expect("A_log", A_log, (H,), torch.float32)
+    if cu_seqlens.dim() != 1 or cu_seqlens.numel() < 1 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be a 1-D int32 tensor [N + 1]")
+    _check_cuda(z, A_log, cu_seqlens, workspace)
     N = cu_seqlens.numel() - 1
     G = torch.empty(T, H, dk, dtype=torch.float32, device=z.device)
     dt = _DT[z.dtype]

@@ -130,6 +130,45 @@ def test_binding_refuses_cpu_tensors(lib):
                         torch.zeros(16, 1, 32, 32))
 
 
+def test_binding_checks_shapes_and_dtypes(lib):
+    """The C ABI takes raw pointers and sizes taken from q (and v): the binding refuses
+    any other tensor whose shape or dtype disagrees, before anything reaches the device."""
+    import torch
+    from gated_delta_rule_43_gb300 import inputs, kda
+    d = inputs.make_prefill([16], H=2, dk=32, dv=32, dtype="f32")
+    args = [d[n] for n in ("q", "k", "v", "z", "beta", "A_log", "cu_seqlens")]
+
+    def with_(i, t):
+        a = list(args)
+        a[i] = t
+        return a
+    with pytest.raises(TypeError, match="k has dtype"):
+        kda.chunk_fwd(*with_(1, d["k"].to(torch.bfloat16)))
+    with pytest.raises(ValueError, match="z has shape"):
+        kda.chunk_fwd(*with_(3, d["z"][:8]))
+    with pytest.raises(ValueError, match="v has shape"):
+        kda.chunk_fwd(*with_(2, d["v"][:, :1].contiguous()))
+    with pytest.raises(ValueError, match="beta has shape"):
+        kda.chunk_fwd(*with_(4, d["beta"][:, :1].contiguous()))
+    with pytest.raises(TypeError, match="A_log has dtype"):
+        kda.chunk_fwd(*with_(5, d["A_log"].to(torch.bfloat16)))
+    with pytest.raises(TypeError, match="cu_seqlens"):
+        kda.chunk_fwd(*with_(6, d["cu_seqlens"].to(torch.int64)))
+    with pytest.raises(ValueError, match="initial_state has shape"):
+        kda.chunk_fwd(*args, torch.zeros(1, 2, 32, 16))
+    with pytest.raises(ValueError, match="o has shape"):
+        kda.chunk_fwd(*args, o=torch.empty(16, 2, 16))
+    with pytest.raises(ValueError, match="final_state has shape"):
+        kda.chunk_fwd_noalloc(*args, None, torch.empty(16, 2, 32), torch.empty(2, 2, 32, 32))
+    with pytest.raises(ValueError, match="state has shape"):
+        kda.decode_step(*args[:6], torch.zeros(16, 2, 32, 16))
+    with pytest.raises(ValueError, match="state_idx has shape"):
+        kda.decode_step_indexed(*args[:6], torch.zeros(20, 2, 32, 32),
+                                torch.zeros(8, dtype=torch.int32))
+    with pytest.raises(ValueError, match="A_log has shape"):
+        kda.gate_cumsum(d["z"], d["A_log"][:1], d["cu_seqlens"])
+
+
 def test_fault_hook_rejects_a_non_positive_limit(lib):
     """The bounded-wait test hook validates its limit on the host (nothing is armed)."""
     from gated_delta_rule_43_gb300 import kda

@@ -148,6 +148,18 @@ def test_both_chain_shapes(lens):
     _run_and_score(d, "bf16")
 
 
+def test_many_short_sequences():
+    """1200 packed sequences of 0-150 tokens (one in ten empty) with initial states: the
+    chunk plan of a large batch and the 128-column chain walking many more items than it
+    has CTAs."""
+    import numpy as np
+    rng = np.random.default_rng(55)
+    lens = [0 if rng.random() < 0.1 else int(rng.integers(1, 151)) for _ in range(1200)]
+    d = inputs.make_prefill(lens, H=4, dk=128, dv=128, dtype="bf16", seed=56, h0_sigma=0.1,
+                            device=DEV)
+    _run_and_score(d, "bf16")
+
+
 @pytest.mark.timeout(900)
 def test_windows_one_head_chain_slower_than_prep():
     """One head, about a million tokens: three windows, each window's prep far shorter than

@@ -4,7 +4,8 @@ Each case draws 1-5 packed sequences whose lengths sit on and around the tile (1
 chunk (64) boundaries or anywhere up to 900 tokens (empty and one-token sequences
 included), 1-5 heads, with or without initial states, and the default or the
 long-memory gate regime.  The bf16 cases at 128/128 run the tensor-core path, the fp32
-ones (head sizes 32, 64 and 128) the CUDA-core path; all are scored over the whole
+ones (head sizes 32, 64 and 128) the CUDA-core path; longer random batches (up to 3000
+tokens a sequence, 8 heads) the tensor-core path again; all are scored over the whole
 tensor within the stated tolerances.  Random decode batches, dense and through a state
 pool, are scored the same way.
 """
@@ -34,6 +35,20 @@ def _case(i: int):
 def test_random_cases_tensor_core_path(i):
     lens, H, h0_sigma, z_shift = _case(i)
     d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=2000 + i,
+                            h0_sigma=h0_sigma, z_shift=z_shift, device=DEV)
+    _run_and_score(d, "bf16")
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_random_long_cases_tensor_core_path(i):
+    """1-6 sequences of up to 3000 tokens (many chunks each), 1-8 heads, three gate regimes."""
+    rng = np.random.default_rng(70000 + i)
+    n = int(rng.integers(1, 7))
+    lens = [int(rng.integers(0, 3001)) for _ in range(n)]
+    H = int(rng.integers(1, 9))
+    h0_sigma = float(rng.choice([0.0, 0.1]))
+    z_shift = float(rng.choice([0.0, -4.0, -6.0]))
+    d = inputs.make_prefill(lens, H=H, dk=128, dv=128, dtype="bf16", seed=71000 + i,
                             h0_sigma=h0_sigma, z_shift=z_shift, device=DEV)
     _run_and_score(d, "bf16")
 
